@@ -1,0 +1,520 @@
+#!/usr/bin/env python
+"""Benchmark of the verification hot path on the 64-request token-level workload.
+
+Workload: 64 requests x 5 drafted positions (+ 1 bonus row), V = 151936, bf16 logits (target
+N(0, 3^2) plus a Zipf(1.1) log-prior, draft = target + N(0, 1)), drafts sampled from q.  One step =
+one spec_verify_token call over the whole batch (row statistics, acceptance walk, correction /
+bonus races).  Inputs (213.9 MB) are larger than L2 and L2 is also flushed (a 512 MB write) before
+every timed step; steps are timed with CUDA events on the launching stream.
+
+Printed: one JSON line (rank 0).  `value` is logit GB/s over the bytes the verifier must read
+(every drafted target and draft row, plus the bonus row of each request that accepted all its
+drafts); `positions_per_s` is drafted positions verified per second.  Supplementary rows time the
+other calls of the library on their own workloads.
+
+--impl reference times the CPU oracle (the plain double-precision restatement of the method) on the
+host cores, on a bounded sample of the same workload, under the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify logits GB/s (% of GB300 HBM peak) and drafted positions verified/sec"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="skip the supplementary rows")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---- environment helpers ---------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_digest():
+    """Digest of the CUDA sources; a stored ncu traffic figure is used only if it matches."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_token_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel_key):
+    """Per-launch DRAM bytes of `kernel_key` from profiles/traffic.json if taken on these sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        data = json.load(f)
+    ent = data.get(kernel_key)
+    if not ent or ent.get("source_digest") != source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- workload -----------------------------------------------------------------------------------
+
+def token_workload(device):
+    import torch
+    import speculative_decoding_verification_token_gb300 as sv
+    from speculative_decoding_verification_token_gb300 import synth
+    w = synth.TOKEN_LARGE
+    inp = synth.token_inputs(w, device=device)
+    tokens = sv.spec_sample_draft(inp["draft"], inp["draft_row0"], inp["draft_len"], w.gamma,
+                                  w.seed)
+    torch.cuda.synchronize()
+    return w, inp, tokens
+
+
+def necessary_bytes(w, accepted_len, esize):
+    """Drafted target + draft rows of every request, plus the bonus row where all were kept."""
+    n_bonus = int((accepted_len == w.gamma).sum())
+    return (2 * w.B * w.gamma + n_bonus) * w.V * esize, n_bonus
+
+
+def time_calls(fn, steps, warmup, flush, stream):
+    import torch
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b) * 1e-3)
+    return times
+
+
+def bench_token(args, rank, world, peaks, peak_src):
+    import torch
+    import speculative_decoding_verification_token_gb300 as sv
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    w, inp, tokens = token_workload(dev)
+    esize = inp["target"].element_size()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = sv.workspace(sv.spec_verify_workspace_bytes(w.B, w.gamma, w.V, sv.SV_BF16), dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    holder = {}
+
+    def step():
+        holder["out"] = sv.spec_verify_token(inp["target"], inp["draft"], inp["target_row0"],
+                                             inp["draft_row0"], inp["draft_len"], w.gamma,
+                                             tokens, w.seed, status=status, workspace=ws)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    with ClockSampler(dev.index) as clocks:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        times = time_calls(step, args.steps, args.warmup, flush, stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+    assert int(status.item()) == 0, sv.status_string(int(status.item()))
+    acc = holder["out"]["accepted_len"].cpu()
+    nbytes, n_bonus = necessary_bytes(w, acc, esize)
+    all_rows_bytes = (2 * w.B * w.gamma + w.B) * w.V * esize
+    t_mean = sum(times) / len(times)
+    total_time = sum(times)
+    if world > 1:
+        tt = torch.tensor([total_time], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_time = float(tt.item())
+    res = {
+        "w": w, "times": times, "t_mean": t_mean, "total_time": total_time,
+        "bytes": nbytes, "all_rows_bytes": all_rows_bytes, "n_bonus": n_bonus,
+        "positions": w.B * w.gamma, "clocks": clocks.summary(), "inp": inp, "tokens": tokens,
+        "accept_mean": float(acc.float().mean()),
+    }
+    return res
+
+
+def bench_e2e(w, inp, tokens, steps, warmup):
+    """The same call fed from pinned host buffers: H2D of the step's logits and layout, verify,
+    D2H of the results, all inside the timed region."""
+    import torch
+    import speculative_decoding_verification_token_gb300 as sv
+    dev = inp["target"].device
+    stream = torch.cuda.current_stream()
+    host = {k: inp[k].cpu().pin_memory() for k in ("target", "draft", "target_row0", "draft_row0",
+                                                     "draft_len")}
+    host["tokens"] = tokens.cpu().pin_memory()
+    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = sv.workspace(sv.spec_verify_workspace_bytes(w.B, w.gamma, w.V, sv.SV_BF16), dev)
+    out_host = {"accepted_len": torch.empty(w.B, dtype=torch.int32).pin_memory(),
+                "out_tokens": torch.empty((w.B, w.gamma + 1), dtype=torch.int32).pin_memory(),
+                "correction": torch.empty(w.B, dtype=torch.int32).pin_memory()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+
+    def step():
+        for k, v in host.items():
+            devb[k].copy_(v, non_blocking=True)
+        out = sv.spec_verify_token(devb["target"], devb["draft"], devb["target_row0"],
+                                   devb["draft_row0"], devb["draft_len"], w.gamma,
+                                   devb["tokens"], w.seed, status=status, workspace=ws)
+        for k in out_host:
+            out_host[k].copy_(out[k], non_blocking=True)
+
+    times = time_calls(step, steps, warmup, lambda: None, stream)
+    return sum(times) / len(times), h2d, d2h, out_host["accepted_len"].clone()
+
+
+# ---- CPU oracle (baseline and reference arm) --------------------------------------------------
+
+def oracle_sample(w, inp, tokens, target_seconds=12.0):
+    """Times the oracle on whole requests of the workload, threads over requests on all host
+    cores, repeating the request set until about `target_seconds` of CPU work is done."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    t = inp["target"].float().cpu().numpy()
+    d = inp["draft"].float().cpu().numpy()
+    tok = tokens.cpu().numpy()
+    lay = {k: inp[k].cpu().numpy() for k in ("target_row0", "draft_row0", "draft_len")}
+    V, G = w.V, w.gamma
+    cores = os.cpu_count() or 1
+
+    def one(r):
+        t0 = lay["target_row0"][r]
+        d0 = lay["draft_row0"][r]
+        res, _ = oracle.verify_token_request(t[t0:t0 + G + 1], d[d0:d0 + G], tok[d0:d0 + G],
+                                             w.seed, r)
+        return res.accepted_len
+
+    # one probe request to size the sample
+    p0 = time.perf_counter()
+    one(0)
+    per_req = time.perf_counter() - p0
+    n_req = max(cores, int(target_seconds / max(per_req, 1e-4)))
+    reqs = [r % w.B for r in range(n_req)]
+    s0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        accs = list(ex.map(one, reqs))
+    wall = time.perf_counter() - s0
+    accs = np.array(accs)
+    n_bonus = int((accs == G).sum())
+    esize = inp["target"].element_size()
+    nbytes = (2 * G * n_req + n_bonus) * V * esize
+    return {"gbs": nbytes / wall / 1e9, "positions_per_s": G * n_req / wall, "cores": cores,
+            "wall_s": wall, "requests": n_req,
+            "sample": f"{n_req} whole requests of the workload (request set repeated), "
+                      f"{G} drafted positions each, V={V}, threads over requests"}
+
+
+# ---- supplementary rows ---------------------------------------------------------------------------
+
+def bench_rows(steps, warmup):
+    import numpy as np
+    import torch
+    import speculative_decoding_verification_token_gb300 as sv
+    from speculative_decoding_verification_token_gb300 import synth
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    rows = {}
+    # block verification, 128 requests x 7, V = 129280
+    w = synth.BLOCK_LARGE
+    inp = synth.token_inputs(w, device=dev)
+    tokens = sv.spec_sample_draft(inp["draft"], inp["draft_row0"], inp["draft_len"], w.gamma,
+                                  w.seed)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = sv.workspace(sv.spec_verify_workspace_bytes(w.B, w.gamma, w.V, sv.SV_BF16), dev)
+    holder = {}
+
+    def blk():
+        holder["o"] = sv.spec_verify_block(inp["target"], inp["draft"], inp["target_row0"],
+                                           inp["draft_row0"], inp["draft_len"], w.gamma, tokens,
+                                           w.seed, status=status, workspace=ws)
+    t = time_calls(blk, steps, warmup, flush, stream)
+    acc = holder["o"]["accepted_len"].cpu()
+    n_bonus = int((acc == w.gamma).sum())
+    nb = (2 * w.B * w.gamma + n_bonus) * w.V * 2
+    tm = sum(t) / len(t)
+    rows["block_verify_128x7_V129280_bf16"] = {
+        "ms": tm * 1e3, "GB_s": nb / tm / 1e9, "positions_per_s": w.B * w.gamma / tm,
+        "mean_accepted": float(acc.float().mean()), "status": int(status.item())}
+    del inp, tokens
+
+    # scheduler, 512 requests x 16 positions
+    sw = synth.SCHEDULE
+    si = synth.schedule_inputs(sw)
+    c = torch.from_numpy(si["cond_accept"]).to(dev)
+    ml = torch.from_numpy(si["max_len"]).to(dev)
+    sps = torch.from_numpy(si["sps"]).to(dev)
+    sched = {}
+
+    def sch():
+        sched["o"] = sv.dspark_schedule(c, ml, sps, si["B_max"], status=status)
+    t = time_calls(sch, steps, warmup, lambda: None, stream)
+    rows["schedule_512x16"] = {"us": sum(t) / len(t) * 1e6,
+                               "total_rows": int(sched["o"]["total_rows"].item()),
+                               "status": int(status.item())}
+
+    # scheduled round: schedule, then verify the selected prefixes (V = 129280)
+    vw = synth.SCHEDULED_VERIFY
+    vin = synth.token_inputs(vw, device=dev)
+    vt = sv.spec_sample_draft(vin["draft"], vin["draft_row0"], vin["draft_len"], vw.gamma,
+                              vw.seed)
+    ws2 = sv.workspace(sv.spec_verify_workspace_bytes(vw.B, vw.gamma, vw.V, sv.SV_BF16), dev)
+    rnd = {}
+
+    def round_():
+        s = sv.dspark_schedule(c, ml, sps, si["B_max"], status=status)
+        rnd["o"] = sv.spec_verify_token(vin["target"], vin["draft"], vin["target_row0"],
+                                        vin["draft_row0"], s["sel_len"], vw.gamma, vt, vw.seed,
+                                        status=status, workspace=ws2)
+        rnd["s"] = s
+    t = time_calls(round_, steps, warmup, flush, stream)
+    sel = rnd["s"]["sel_len"].cpu()
+    acc = rnd["o"]["accepted_len"].cpu()
+    n_bonus = int((acc == sel).sum())
+    nb = (2 * int(sel.sum()) + n_bonus) * vw.V * 2
+    tm = sum(t) / len(t)
+    rows["scheduled_round_512x16_V129280_bf16"] = {
+        "ms": tm * 1e3, "GB_s": nb / tm / 1e9, "positions_per_s": int(sel.sum()) / tm,
+        "verified_rows": int(rnd["s"]["total_rows"].item()), "status": int(status.item())}
+    return rows
+
+
+# ---- main ----------------------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    peaks, peak_src = measured_peaks()
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+        __graft_entry__.build()
+
+    res = bench_token(args, rank, world, peaks, peak_src)
+    w = res["w"]
+    value = res["bytes"] * world / res["total_time"] * args.steps / 1e9
+    pos_s = res["positions"] * world * args.steps / res["total_time"]
+    hbm = float(peaks["hbm_gbs"])
+    achieved = res["bytes"] / res["t_mean"] / 1e9
+    e2e_t, h2d, d2h, _ = bench_e2e(w, res["inp"], res["tokens"], max(3, args.steps // 3),
+                                   max(3, args.warmup))
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(res["t_mean"] * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "token-level verify, 64 requests x 5 drafted positions + bonus, "
+                               "V=151936, bf16 logits (target N(0,9) + Zipf(1.1) prior, draft = "
+                               "target + N(0,1)), drafts sampled from q",
+                   "B": w.B, "gamma": w.gamma, "V": w.V,
+                   "l2": "inputs (213.9 MB) larger than L2, and L2 flushed by a 512 MB write "
+                         "before every step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "positions_per_s": round(pos_s, 1),
+        "hbm_frac_of_measured": round(achieved / hbm, 4),
+        "bytes_per_step": res["bytes"],
+        "bytes_all_rows_per_step": res["all_rows_bytes"],
+        "bonus_rows_read": res["n_bonus"],
+        "mean_accepted_len": round(res["accept_mean"], 3),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": stored_traffic("token_verify_64x5_V151936"),
+                     "kernel": "spec_verify_token call (plan + stream + final kernels)",
+                     "peak_source": peak_src},
+        "e2e": {"value": round(res["bytes"] / e2e_t / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_t * 1e3, 4)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": res["clocks"],
+    }
+    if not args.no_rows and rank == 0:
+        line["rows"] = bench_rows(max(5, args.steps // 3), max(3, args.warmup))
+    if not args.no_cpu_baseline and rank == 0:
+        cpu = oracle_sample(w, res["inp"], res["tokens"])
+        line["cpu_baseline"] = {"value": round(cpu["gbs"], 4), "unit": "GB/s",
+                                "cores": cpu["cores"], "kind": "oracle",
+                                "sample": cpu["sample"],
+                                "positions_per_s": round(cpu["positions_per_s"], 2)}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args, rank, world):
+    """CPU oracle under the same metric: each step is a bounded sample of the workload."""
+    if rank != 0:
+        return
+    import torch
+    from speculative_decoding_verification_token_gb300 import synth
+    import oracle
+    oracle.build()
+    w = synth.TOKEN_LARGE
+    inp = synth.token_inputs(w, device="cpu")
+    t = inp["target"].float().numpy()
+    d = inp["draft"].float().numpy()
+    lay = {k: inp[k].numpy() for k in ("target_row0", "draft_row0", "draft_len")}
+    st, tokens = oracle.sample_draft_batch(d, w.V, w.V, lay["draft_row0"], lay["draft_len"], w.B,
+                                           w.seed)
+    cores = os.cpu_count() or 1
+    n_req = min(w.B, max(cores, 16))
+    import numpy as np
+
+    def one(r):
+        t0, d0 = lay["target_row0"][r], lay["draft_row0"][r]
+        res, _ = oracle.verify_token_request(t[t0:t0 + w.gamma + 1], d[d0:d0 + w.gamma],
+                                             tokens[d0:d0 + w.gamma], w.seed, r)
+        return res.accepted_len
+
+    def step():
+        with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+            return np.array(list(ex.map(one, range(n_req))))
+
+    for _ in range(args.warmup):
+        step()
+    times, byts = [], []
+    for _ in range(args.steps):
+        s0 = time.perf_counter()
+        acc = step()
+        times.append(time.perf_counter() - s0)
+        byts.append((2 * w.gamma * n_req + int((acc == w.gamma).sum())) * w.V * 2)
+    tot = sum(times)
+    value = sum(byts) / tot / 1e9
+    sample = (f"{n_req} of the 64 requests per step ({w.gamma} drafted positions each, "
+              f"V={w.V}), threads over requests")
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "token-level verify, 64 requests x 5 drafted positions + "
+                                   "bonus, V=151936, bf16 logits", "B": w.B, "gamma": w.gamma,
+                       "V": w.V},
+            "impl": "reference",
+            "positions_per_s": round(w.gamma * n_req * args.steps / tot, 2),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * specverify.h -- C ABI of the GB300 speculative-decoding verification library.
+ *
+ * The library turns target and draft logits into verified tokens (token-level and block
+ * verification), drafts a block with DSpark's Markov head, and schedules how much of each drafted
+ * block to verify.  Every call is one or more hand-written CUDA kernels for sm_103a launched on the
+ * caller's stream.
+ *
+ * Conventions for every entry point
+ *   - Pointers marked DEVICE are device pointers owned by the caller; HOST pointers are read
+ *     synchronously during the call.  The library allocates no memory and keeps no state between
+ *     calls.  Scratch memory is the caller's `workspace` (DEVICE, 256-byte aligned), sized by the
+ *     matching *_workspace_bytes query; its contents need no initialisation and are clobbered.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are asynchronous: they
+ *     return after launching; outputs are valid once the stream reaches that point.
+ *   - Argument errors (bad sizes, NULL required pointers, misaligned rows, a too-small workspace)
+ *     return SV_ERR_INVALID / SV_ERR_UNSUPPORTED synchronously and launch nothing.
+ *   - Data errors found on the device (token id outside [0, V), NaN or +inf logits, an all -inf
+ *     row, q(x) = 0 for the drafted token x, a drafted length outside [0, max_draft_len]) are
+ *     written to the optional DEVICE word `status` (reset to SV_OK by each call; the first error
+ *     found is kept).  Outputs are then undefined.  `status` is NULL -> data errors go unreported.
+ *   - A device-side wait that exceeds its bound writes SV_ERR_TIMEOUT to `status`.
+ *   - Logits may hold -inf (masked tokens); such tokens are never emitted.
+ *   - Rows are `ld` elements apart; the row base addresses must be 16-byte aligned, i.e. the logit
+ *     pointers 16-byte aligned and ld * sizeof(element) a multiple of 16.  V itself is arbitrary.
+ *
+ * Random numbers: uniforms come from Philox4x32-10 (Salmon et al., SC'11, "Parallel Random
+ * Numbers: As Easy as 1, 2, 3") with key (lo32(seed), hi32(seed)) and counter
+ * (v >> 2, position, lo32(request id), tag << 24 | (hi32(request id) & 0xFFFFFF)), word v & 3,
+ * converted as u = ((word >> 9) + 0.5) * 2^-23 (never 0 or 1).  Tags: DRAFT 0, ACCEPT 1, RESID 2,
+ * BONUS 3.  Positions are 1-based: drafted tokens at 1..gamma, the bonus row at gamma + 1.
+ * Every sample is an exponential race: x = argmax_x log w(x) - log(-log u_x), which draws x with
+ * probability w(x) / sum(w) without a normalisation pass; equal keys go to the lower index.
+ *
+ * Sources (web pages, by title and section):
+ *   "Speculative Decoding: The Same Distribution, Twice as Fast" §3 "The loop", §4 "The rule that
+ *     makes it exact" (accept with min(1, p/q); correction from max(0, p - q) renormalised).
+ *   "How much does a token cost", "On Speculative Sampling" (the same rule; Panels A-C) and "Block
+ *     verification" (running target-to-draft ratio capped at one; longest passing prefix).
+ *   "DeepSeek DSpark 详解" §03 (Markov head: a rank-256 low-rank transition from the previous
+ *     sampled token corrects the parallel backbone's logits, left to right) and §04 (confidence
+ *     head, prefix survival = product of conditional acceptance probabilities, sequential
+ *     temperature scaling, maximise expected accepted tokens x SPS(B), early stop).
+ *   "DSpark: DeepSeek's bet on speed that doesn't betray quality", "Verifying only what matters".
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_INVALID = 1,      /* invalid argument (returned synchronously) */
+  SV_ERR_UNSUPPORTED = 2,  /* valid but unsupported argument (returned synchronously) */
+  SV_ERR_CUDA = 3,         /* a CUDA runtime call failed (returned synchronously) */
+  SV_ERR_BAD_INPUT = 4,    /* data error found on the device (written to *status) */
+  SV_ERR_TIMEOUT = 5       /* a bounded device-side wait expired (written to *status) */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* Largest drafted length per request accepted by the verify calls and the Markov head. */
+#define SV_MAX_DRAFT_LEN 64
+
+/* Human-readable name of a status code (static string). */
+const char* sv_status_string(sv_status status);
+
+/* Library build identifier (static string), e.g. for logs. */
+const char* sv_version(void);
+
+/* ---------------------------------------------------------------------------------------------
+ * Verification.
+ *
+ * Layout (all DEVICE unless noted).  Request r (0 <= r < B) drafted gamma_r = draft_len[r]
+ * tokens.  Its target rows are target_row0[r] + 0 .. gamma_r (row i-1 scores position i, row
+ * gamma_r is the bonus row) and its draft rows draft_row0[r] + 0 .. gamma_r - 1, all in units of
+ * rows of `ld` elements of `dtype`.  Its drafted token at position i is
+ * draft_tokens[draft_row0[r] + i - 1] (the token array is indexed like the draft rows).
+ * `max_draft_len` (HOST value) bounds every gamma_r and sizes the workspace.
+ * request_ids (nullable, [B] uint64): the request id that keys the uniforms; NULL means r.
+ *
+ * Outputs: accepted_len[B] = tau_r; out_tokens[B * out_ld] (out_ld >= max_draft_len + 1) holds
+ * x_1 .. x_tau, then the correction (or bonus) token, then -1; correction_token[B] (nullable) the
+ * last emitted token.
+ * ------------------------------------------------------------------------------------------- */
+
+/* Workspace bytes needed by spec_verify_token / spec_verify_block / spec_sample_draft. */
+size_t spec_verify_workspace_bytes(int32_t B, int32_t max_draft_len, int64_t V, sv_dtype dtype);
+
+/* Token-level speculative sampling ("Speculative Decoding: The Same Distribution, Twice as Fast"
+ * §4; "How much does a token cost", "On Speculative Sampling").  For i = 1..gamma_r:
+ * rho_i = p_i(x_i) / q_i(x_i) with p_i = softmax(target row i), q_i = softmax(draft row i);
+ * accept iff u_i < rho_i (u_i: ACCEPT tag, position i).  tau = (first rejected i) - 1, or gamma_r.
+ * On a rejection the correction is raced from max(p_{tau+1} - q_{tau+1}, 0) (RESID tag, position
+ * tau + 1; if that residual is empty to working precision, from p_{tau+1} with the same
+ * uniforms); otherwise the bonus token is raced from p_{gamma+1} (BONUS tag, position gamma + 1).
+ * accept_ratio (nullable, indexed like draft_tokens): min(1, rho_i) for EVERY drafted position. */
+sv_status spec_verify_token(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                            int64_t V, int64_t ld, const int64_t* target_row0,
+                            const int64_t* draft_row0, const int32_t* draft_len,
+                            int32_t max_draft_len, const int32_t* draft_tokens, int32_t B,
+                            uint64_t seed, const uint64_t* request_ids, int32_t* accepted_len,
+                            int32_t* out_tokens, int64_t out_ld, int32_t* correction_token,
+                            float* accept_ratio, int32_t* status, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Block verification ("How much does a token cost", "Block verification": the running ratio
+ * starts at one, is multiplied by p/q at every drafted token and capped at one after every step;
+ * all prefixes are checked and the longest passing one is kept; its acceptance thresholds and
+ * correction sampling are those of Sun et al. 2024, "Block Verification Accelerates Speculative
+ * Decoding", whose two-token toy the page reproduces):
+ *   rho_0 = 1, rho_i = min(1, rho_{i-1} p_i(x_i) / q_i(x_i))
+ *   R_i = sum_x max(rho_i p_{i+1}(x) - q_{i+1}(x), 0) for i < gamma
+ *   h_i = R_i / (R_i + 1 - rho_i) for i < gamma (1 if the denominator is 0), h_gamma = rho_gamma
+ *   tau = max{i : eta_i <= h_i} or 0 (eta_i: ACCEPT tag, position i)
+ *   tau < gamma: correction raced from max(rho_tau p_{tau+1} - q_{tau+1}, 0) (RESID, tau + 1)
+ *   tau = gamma: bonus raced from p_{gamma+1} (BONUS, gamma + 1).
+ * running_ratio, h_threshold (nullable, indexed like draft_tokens): rho_i and h_i. */
+sv_status spec_verify_block(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                            int64_t V, int64_t ld, const int64_t* target_row0,
+                            const int64_t* draft_row0, const int32_t* draft_len,
+                            int32_t max_draft_len, const int32_t* draft_tokens, int32_t B,
+                            uint64_t seed, const uint64_t* request_ids, int32_t* accepted_len,
+                            int32_t* out_tokens, int64_t out_ld, int32_t* correction_token,
+                            float* running_ratio, float* h_threshold, int32_t* status,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Draft tokens sampled from q ("Speculative Decoding: The Same Distribution, Twice as Fast" §3
+ * step 1, the drafter's own sampling): for every request r and i = 1..gamma_r,
+ * draft_tokens[draft_row0[r] + i - 1] = race sample of softmax(draft row draft_row0[r] + i - 1)
+ * with the DRAFT tag at position i.  Layout and workspace as for spec_verify_token. */
+sv_status spec_sample_draft(const void* draft_logits, sv_dtype dtype, int64_t V, int64_t ld,
+                            const int64_t* draft_row0, const int32_t* draft_len,
+                            int32_t max_draft_len, int32_t B, uint64_t seed,
+                            const uint64_t* request_ids, int32_t* draft_tokens, int32_t* status,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * DSpark draft side.
+ * ------------------------------------------------------------------------------------------- */
+
+/* Workspace bytes needed by dspark_markov_draft. */
+size_t dspark_markov_workspace_bytes(int32_t B, int32_t K, int64_t V, int32_t R);
+
+/* Markov-head drafting ("DeepSeek DSpark 详解" §03; "How much does a token cost", "DSpark
+ * Architecture"): x_0 = anchor_token[b]; for k = 1..K, left to right,
+ *   z_k = bf16( backbone_k + U[x_{k-1}] . W )      (bf16 operands, fp32 accumulation)
+ *   x_k = argmax_v z_k(v) - log(-log u_v)           (DRAFT tag, position k)
+ *   conf_k = 1 / (1 + exp(-conf_scores[b][k] / sts_T[k]))   (sequential temperature scaling)
+ * backbone_logits: DEVICE bf16 [B][K][V], row (b, k) at (b * K + k) * ldb elements;
+ * U: DEVICE bf16 [V][R] (row stride R); W: DEVICE bf16 [R][V] (row stride ldw);
+ * anchor_token: DEVICE int32 [B]; conf_scores: DEVICE fp32 [B][K]; sts_T: DEVICE fp32 [K].
+ * R must be 256 (SV_ERR_UNSUPPORTED otherwise); 1 <= K <= SV_MAX_DRAFT_LEN.
+ * Outputs: draft_tokens DEVICE int32 [B][K]; draft_logits_out (nullable) DEVICE bf16 [B][K][V]
+ * with row stride ldz -- the exact rows the tokens were sampled from, to be passed to verify;
+ * row_stats (nullable) fp32 [B][K][2] = (max z, log-sum-exp z); conf_out (nullable) fp32 [B][K].
+ * request_ids as for verify.  ldb, ldw, ldz: multiples of 8 elements. */
+sv_status dspark_markov_draft(const void* backbone_logits, int64_t ldb, const void* U,
+                              const void* W, int64_t ldw, const int32_t* anchor_token,
+                              const float* conf_scores, const float* sts_T, int32_t B, int32_t K,
+                              int64_t V, int32_t R, uint64_t seed, const uint64_t* request_ids,
+                              int32_t* draft_tokens, void* draft_logits_out, int64_t ldz,
+                              float* row_stats, float* conf_out, int32_t* status,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes needed by dspark_schedule. */
+size_t dspark_schedule_workspace_bytes(int32_t N, int32_t K);
+
+/* Hardware-aware prefix scheduler ("DeepSeek DSpark 详解" §04; "DSpark: DeepSeek's bet on speed
+ * that doesn't betray quality", "Verifying only what matters"):
+ *   S[i][k] = c[i][1] * ... * c[i][k]  (sequential binary32 products, k <= max_len[i])
+ *   extendable prefixes (i, k) sorted by S descending, then k ascending, then i ascending;
+ *   F = floor(S * 2^40); T(b) = N * 2^40 + (sum of F over the first b);
+ *   f(b) = (double) T(b) * 2^-40 * sps[N + b];
+ *   admit while f(b + 1) > f(b) and N + b + 1 <= B_max, stopping at the first non-increase.
+ * cond_accept: DEVICE fp32 [N][K] in [0, 1] (calibrated conditional acceptance probabilities);
+ * max_len: DEVICE int32 [N] in [0, K] (nullable -> K); sps: DEVICE fp64 [B_max + 1], engine steps
+ * per second at B verification rows (one row per request plus admitted drafts).
+ * Outputs: sel_len DEVICE int32 [N] (drafts to verify per request); survival (nullable) fp32
+ * [N][K] (0 past max_len); total_rows DEVICE int32 [1] = N + b; objective DEVICE fp64 [1] = f(b).
+ * Supported sizes: N * K <= 16384, N <= B_max. */
+sv_status dspark_schedule(const float* cond_accept, const int32_t* max_len, int32_t N, int32_t K,
+                          const double* sps, int32_t B_max, int32_t* sel_len, float* survival,
+                          int32_t* total_rows, double* objective, int32_t* status,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

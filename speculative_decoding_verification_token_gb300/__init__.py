@@ -1,0 +1,287 @@
+"""GB300 speculative-decoding verification: Python binding of ``libspecverify.so``.
+
+The functions below carry the names of the C entry points declared in ``include/specverify.h`` and
+do argument marshalling only: every step runs in the library's CUDA kernels.  Tensors must live on
+the current CUDA device; outputs that are not supplied are allocated with torch.  The library is
+loaded on first use and its absence raises -- there is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "specverify.h")
+
+SV_OK, SV_ERR_INVALID, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_BAD_INPUT, SV_ERR_TIMEOUT = range(6)
+SV_F32, SV_BF16 = 0, 1
+SV_MAX_DRAFT_LEN = 64
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)}")
+
+
+def declared_functions():
+    """Names of the functions declared in include/specverify.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*"
+                                 r"([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)))
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = C.CDLL(LIB_PATH)
+        P, i32, i64, u64, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_size_t
+        st = C.c_int
+        verify_args = [P, P, st, i64, i64, P, P, P, i32, P, i32, u64, P, P, P, i64, P]
+        sigs = {
+            "sv_status_string": (C.c_char_p, [st]),
+            "sv_version": (C.c_char_p, []),
+            "spec_verify_workspace_bytes": (sz, [i32, i32, i64, st]),
+            "spec_verify_token": (st, verify_args + [P, P, P, sz, P]),
+            "spec_verify_block": (st, verify_args + [P, P, P, P, sz, P]),
+            "spec_sample_draft": (st, [P, st, i64, i64, P, P, i32, i32, u64, P, P, P, P, sz, P]),
+            "dspark_markov_workspace_bytes": (sz, [i32, i32, i64, i32]),
+            "dspark_markov_draft": (st, [P, i64, P, P, i64, P, P, P, i32, i32, i64, i32, u64, P,
+                                         P, P, i64, P, P, P, P, sz, P]),
+            "dspark_schedule_workspace_bytes": (sz, [i32, i32]),
+            "dspark_schedule": (st, [P, P, i32, i32, P, i32, P, P, P, P, P, P, sz, P]),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+        return L
+
+
+def status_string(code):
+    return lib().sv_status_string(int(code)).decode()
+
+
+def version():
+    return lib().sv_version().decode()
+
+
+def _check(code, where):
+    if code != SV_OK:
+        raise SpecVerifyError(code, where)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    if t.dtype == torch.float32:
+        return SV_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _dev(t, dtype=None, rows=False):
+    """Checks a device tensor; `rows` allows a row-strided 2-D view (logits with ld > V)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the library must be on a CUDA device")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {t.dtype}")
+    if rows:
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("logits must be a 2-D tensor with unit column stride")
+    elif not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return t
+
+
+_ws_cache = {}
+
+
+def workspace(nbytes, device=None):
+    """A cached device buffer of at least `nbytes` bytes (256-byte aligned, from torch)."""
+    device = torch.device(device or torch.cuda.current_device())
+    key = (device.index, threading.get_ident())
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+# ---- verification ----------------------------------------------------------------------------
+
+def spec_verify_workspace_bytes(B, max_draft_len, V, dtype_code):
+    return int(lib().spec_verify_workspace_bytes(B, max_draft_len, V, dtype_code))
+
+
+def _verify(block, target, draft, target_row0, draft_row0, draft_len, max_draft_len,
+            draft_tokens, seed, request_ids, out_ld, want_rows, status, ws, stream):
+    _dev(target, rows=True), _dev(draft, rows=True)
+    _dev(target_row0, torch.int64), _dev(draft_row0, torch.int64)
+    _dev(draft_len, torch.int32), _dev(draft_tokens, torch.int32)
+    _dev(request_ids)
+    dt = _dtype_code(target)
+    if draft.dtype != target.dtype:
+        raise TypeError("target and draft logits must have the same dtype")
+    V = target.shape[-1]
+    ld = target.stride(0)
+    if draft.stride(0) != ld:
+        raise ValueError("target and draft rows must have the same stride")
+    B = draft_len.numel()
+    out_ld = out_ld or max_draft_len + 1
+    dev = target.device
+    accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    out_tokens = torch.empty((B, out_ld), dtype=torch.int32, device=dev)
+    correction = torch.empty(B, dtype=torch.int32, device=dev)
+    n_draft_rows = draft_tokens.numel()
+    rows_a = torch.empty(n_draft_rows, dtype=torch.float32, device=dev) if want_rows else None
+    rows_h = (torch.empty(n_draft_rows, dtype=torch.float32, device=dev)
+              if (want_rows and block) else None)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    need = spec_verify_workspace_bytes(B, max_draft_len, V, dt)
+    if ws is None:
+        ws = workspace(need, dev)
+    args = [_ptr(target), _ptr(draft), dt, V, ld, _ptr(target_row0), _ptr(draft_row0),
+            _ptr(draft_len), int(max_draft_len), _ptr(draft_tokens), B, int(seed),
+            _ptr(request_ids), _ptr(accepted), _ptr(out_tokens), out_ld, _ptr(correction)]
+    if block:
+        code = lib().spec_verify_block(*args, _ptr(rows_a), _ptr(rows_h), _ptr(status),
+                                       _ptr(ws), ws.numel(), _stream(stream))
+    else:
+        code = lib().spec_verify_token(*args, _ptr(rows_a), _ptr(status), _ptr(ws), ws.numel(),
+                                       _stream(stream))
+    _check(code, "spec_verify_block" if block else "spec_verify_token")
+    out = {"accepted_len": accepted, "out_tokens": out_tokens, "correction": correction,
+           "status": status}
+    if block:
+        out["running_ratio"] = rows_a
+        out["h"] = rows_h
+    else:
+        out["accept_ratio"] = rows_a
+    return out
+
+
+def spec_verify_token(target, draft, target_row0, draft_row0, draft_len, max_draft_len,
+                      draft_tokens, seed, request_ids=None, out_ld=None, want_ratio=True,
+                      status=None, workspace=None, stream=None):
+    """Token-level verification (see include/specverify.h).  Returns a dict of device tensors."""
+    return _verify(False, target, draft, target_row0, draft_row0, draft_len, max_draft_len,
+                   draft_tokens, seed, request_ids, out_ld, want_ratio, status, workspace, stream)
+
+
+def spec_verify_block(target, draft, target_row0, draft_row0, draft_len, max_draft_len,
+                      draft_tokens, seed, request_ids=None, out_ld=None, want_rows=True,
+                      status=None, workspace=None, stream=None):
+    """Block verification (see include/specverify.h).  Returns a dict of device tensors."""
+    return _verify(True, target, draft, target_row0, draft_row0, draft_len, max_draft_len,
+                   draft_tokens, seed, request_ids, out_ld, want_rows, status, workspace, stream)
+
+
+def spec_sample_draft(draft, draft_row0, draft_len, max_draft_len, seed, request_ids=None,
+                      draft_tokens=None, status=None, workspace=None, stream=None):
+    """Sample draft tokens from q for every drafted row; returns the token tensor (by draft row)."""
+    _dev(draft, rows=True), _dev(draft_row0, torch.int64), _dev(draft_len, torch.int32)
+    dt = _dtype_code(draft)
+    V = draft.shape[-1]
+    ld = draft.stride(0)
+    B = draft_len.numel()
+    dev = draft.device
+    if draft_tokens is None:
+        draft_tokens = torch.full((draft.shape[0],), -1, dtype=torch.int32, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    need = spec_verify_workspace_bytes(B, max_draft_len, V, dt)
+    ws = workspace if workspace is not None else globals()["workspace"](need, dev)
+    code = lib().spec_sample_draft(_ptr(draft), dt, V, ld, _ptr(draft_row0), _ptr(draft_len),
+                                   int(max_draft_len), B, int(seed), _ptr(request_ids),
+                                   _ptr(draft_tokens), _ptr(status), _ptr(ws), ws.numel(),
+                                   _stream(stream))
+    _check(code, "spec_sample_draft")
+    return draft_tokens
+
+
+# ---- DSpark draft side ------------------------------------------------------------------------
+
+def dspark_markov_workspace_bytes(B, K, V, R):
+    return int(lib().dspark_markov_workspace_bytes(B, K, V, R))
+
+
+def dspark_markov_draft(backbone, U, W, anchor, conf_scores, sts_T, seed, request_ids=None,
+                        want_logits=True, want_stats=True, status=None, workspace=None,
+                        stream=None):
+    """Markov-head drafting.  backbone bf16 [B, K, V]; U bf16 [V, R]; W bf16 [R, V]."""
+    _dev(backbone, torch.bfloat16), _dev(U, torch.bfloat16), _dev(W, torch.bfloat16)
+    _dev(anchor, torch.int32), _dev(conf_scores, torch.float32), _dev(sts_T, torch.float32)
+    B, K, V = backbone.shape
+    R = U.shape[1]
+    dev = backbone.device
+    tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
+    z = torch.empty((B, K, V), dtype=torch.bfloat16, device=dev) if want_logits else None
+    stats = torch.empty((B, K, 2), dtype=torch.float32, device=dev) if want_stats else None
+    conf = torch.empty((B, K), dtype=torch.float32, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    need = dspark_markov_workspace_bytes(B, K, V, R)
+    ws = workspace if workspace is not None else globals()["workspace"](need, dev)
+    code = lib().dspark_markov_draft(_ptr(backbone), V, _ptr(U), _ptr(W), W.stride(0),
+                                     _ptr(anchor), _ptr(conf_scores), _ptr(sts_T), B, K, V, R,
+                                     int(seed), _ptr(request_ids), _ptr(tokens), _ptr(z),
+                                     V, _ptr(stats), _ptr(conf), _ptr(status), _ptr(ws),
+                                     ws.numel(), _stream(stream))
+    _check(code, "dspark_markov_draft")
+    return {"draft_tokens": tokens, "draft_logits": z, "row_stats": stats, "conf": conf,
+            "status": status}
+
+
+def dspark_schedule_workspace_bytes(N, K):
+    return int(lib().dspark_schedule_workspace_bytes(N, K))
+
+
+def dspark_schedule(cond_accept, max_len, sps, B_max, want_survival=True, status=None,
+                    workspace=None, stream=None):
+    """Hardware-aware prefix scheduler.  cond_accept fp32 [N, K]; sps fp64 [B_max + 1]."""
+    _dev(cond_accept, torch.float32), _dev(max_len, torch.int32), _dev(sps, torch.float64)
+    N, K = cond_accept.shape
+    dev = cond_accept.device
+    sel = torch.empty(N, dtype=torch.int32, device=dev)
+    surv = torch.empty((N, K), dtype=torch.float32, device=dev) if want_survival else None
+    total = torch.empty(1, dtype=torch.int32, device=dev)
+    obj = torch.empty(1, dtype=torch.float64, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    need = dspark_schedule_workspace_bytes(N, K)
+    ws = workspace if workspace is not None else globals()["workspace"](need, dev)
+    code = lib().dspark_schedule(_ptr(cond_accept), _ptr(max_len), N, K, _ptr(sps), int(B_max),
+                                 _ptr(sel), _ptr(surv), _ptr(total), _ptr(obj), _ptr(status),
+                                 _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "dspark_schedule")
+    return {"sel_len": sel, "survival": surv, "total_rows": total, "objective": obj,
+            "status": status}

@@ -1,0 +1,47 @@
+// api.cu -- status strings, version and the host-side device queries used by every entry point.
+#include <mutex>
+
+#include "sv_host.h"
+
+namespace sv {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sm_count[kMaxDevices] = {0};
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+int resident_ctas(const void* kernel, int threads, size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+}  // namespace sv
+
+extern "C" const char* sv_status_string(sv_status status) {
+  switch (status) {
+    case SV_OK: return "SV_OK";
+    case SV_ERR_INVALID: return "SV_ERR_INVALID: invalid argument";
+    case SV_ERR_UNSUPPORTED: return "SV_ERR_UNSUPPORTED: unsupported argument";
+    case SV_ERR_CUDA: return "SV_ERR_CUDA: CUDA runtime error";
+    case SV_ERR_BAD_INPUT: return "SV_ERR_BAD_INPUT: invalid data found on the device";
+    case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: bounded device-side wait expired";
+  }
+  return "unknown sv_status";
+}
+
+extern "C" const char* sv_version(void) { return "specverify 0.1 (sm_103a)"; }

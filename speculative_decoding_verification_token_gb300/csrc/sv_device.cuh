@@ -1,0 +1,285 @@
+// sv_device.cuh -- device building blocks shared by the verification, drafting and scheduling
+// kernels: the Philox4x32-10 counter generator, exponential-race keys, bulk-copy / mbarrier PTX,
+// online softmax statistics and block reductions.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "specverify.h"
+
+namespace sv {
+
+constexpr int kThreads = 256;               // threads of every streaming CTA
+constexpr int kWarps = kThreads / 32;
+constexpr uint32_t kSliceBytes = 16384;     // one row slice staged in shared memory
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// Upper bound of -log(E) over every uniform the generator can produce: the largest uniform is
+// 1 - 2^-24, for which E = -log(u) ~ 5.96e-8 and -log(E) ~ 16.6355; the bound leaves room for
+// rounding.  A race entry whose log-weight plus this bound is below the best key so far cannot win.
+constexpr float kMaxNoise = 16.75f;
+
+enum : uint32_t { kTagDraft = 0, kTagAccept = 1, kTagResid = 2, kTagBonus = 3 };
+
+// ---- Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11, "Parallel Random Numbers: As Easy as
+// 1, 2, 3", section 3.3): ten rounds of the 4x32 S-box; the round multipliers act on words 0 and
+// 2, their high halves are xored with the odd words and the round key, and the key advances by the
+// Weyl increments after every round.
+__device__ __forceinline__ uint4 philox_block(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint32_t m0 = 0xD2511F53u, m1 = 0xCD9E8D57u;
+    const uint32_t hi0 = __umulhi(m0, c.x), lo0 = m0 * c.x;
+    const uint32_t hi1 = __umulhi(m1, c.z), lo1 = m1 * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// One stream of uniforms: key (lo32(seed), hi32(seed)); counter (v >> 2, pos, lo32(req),
+// tag << 24 | hi32(req) & 0xFFFFFF); vocabulary entry v reads word v & 3.
+struct Stream {
+  uint32_t k0, k1, pos, req_lo, hi;
+};
+
+__device__ __forceinline__ Stream make_stream(uint64_t seed, uint64_t req, uint32_t pos,
+                                              uint32_t tag) {
+  Stream s;
+  s.k0 = static_cast<uint32_t>(seed);
+  s.k1 = static_cast<uint32_t>(seed >> 32);
+  s.pos = pos;
+  s.req_lo = static_cast<uint32_t>(req);
+  s.hi = (tag << 24) | (static_cast<uint32_t>(req >> 32) & 0xFFFFFFu);
+  return s;
+}
+
+__device__ __forceinline__ uint4 stream_block(const Stream& s, uint32_t group) {
+  return philox_block(make_uint4(group, s.pos, s.req_lo, s.hi), s.k0, s.k1);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& b, uint32_t lane) {
+  return lane == 0 ? b.x : lane == 1 ? b.y : lane == 2 ? b.z : b.w;
+}
+
+// u = ((w >> 9) + 1/2) * 2^-23, exact in binary32, inside (0, 1).
+__device__ __forceinline__ float uniform_of(uint32_t w) {
+  return (static_cast<float>(w >> 9) + 0.5f) * 1.1920928955078125e-07f;
+}
+
+// -log(E) with E = -log(u) the exponential variable of a race entry.  Accurate logf: race winners
+// have u close to 1, where E must keep its relative precision.
+__device__ __forceinline__ float race_noise(float u) { return -logf(-logf(u)); }
+
+// ---- status word ---------------------------------------------------------------------------
+__device__ __forceinline__ void report(int32_t* status, int32_t code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// ---- shared-memory addressing, mbarriers and bulk copies (PTX) ----------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Make barrier initialisation visible to the asynchronous (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Order earlier generic-proxy accesses of shared memory before later bulk copies into it.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Bulk copy global -> shared completing on `bar` (src, dst 16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of `bar` for at most ~1 s; on expiry report SV_ERR_TIMEOUT and give up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > 1000000000ull) {
+      report(status, SV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// ---- element access ---------------------------------------------------------------------------
+template <typename E>
+struct Elem;
+
+template <>
+struct Elem<float> {
+  static constexpr int kPerVec = 4;
+  __device__ static __forceinline__ float load(const void* base, int64_t i) {
+    return __ldg(reinterpret_cast<const float*>(base) + i);
+  }
+  __device__ static __forceinline__ void unpack(const uint4& v, float* x) {
+    x[0] = __uint_as_float(v.x);
+    x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z);
+    x[3] = __uint_as_float(v.w);
+  }
+};
+
+struct bf16_tag {};
+
+template <>
+struct Elem<bf16_tag> {
+  static constexpr int kPerVec = 8;
+  __device__ static __forceinline__ float load(const void* base, int64_t i) {
+    const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(base) + i);
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+  __device__ static __forceinline__ void unpack(const uint4& v, float* x) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = __uint_as_float(w[j] << 16);
+      x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 1 - exp(y) for y <= 0, accurate relative to the result: near 0 the Taylor series of -expm1,
+// -y (1 + y/2! + y^2/3! + ... + y^7/8!) (truncation below 1.1e-8 relative for |y| <= 1/2); below
+// -1/2 the difference 1 - 2^(y log2 e) keeps all but 1.4 bits of the result.
+__device__ __forceinline__ float one_minus_exp(float y) {
+  if (y > -0.5f) {
+    float p = 2.48015873015873e-05f;           // 1/8!
+    p = fmaf(p, y, 1.984126984126984e-04f);    // 1/7!
+    p = fmaf(p, y, 1.388888888888889e-03f);    // 1/6!
+    p = fmaf(p, y, 8.333333333333333e-03f);    // 1/5!
+    p = fmaf(p, y, 4.166666666666666e-02f);    // 1/4!
+    p = fmaf(p, y, 1.666666666666667e-01f);    // 1/3!
+    p = fmaf(p, y, 0.5f);                      // 1/2!
+    p = fmaf(p, y, 1.0f);
+    return -y * p;
+  }
+  return 1.0f - fast_exp2(y * kLog2e);
+}
+
+// ---- online softmax statistics: (m, s) = (running max, sum of exp(x - m)) ----------------------
+__device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) {  // both empty (all -inf so far)
+    s = s + s2;           // keeps a NaN visible
+    return;
+  }
+  s = s * fast_exp2((m - mn) * kLog2e) + s2 * fast_exp2((m2 - mn) * kLog2e);
+  m = mn;
+}
+
+// Fold `n` values into (m, s): one rescale per increase of the maximum, one exp per value.
+template <int N>
+__device__ __forceinline__ void ms_accumulate(float& m, float& s, const float* x) {
+  float cm = x[0];
+#pragma unroll
+  for (int j = 1; j < N; ++j) cm = fmaxf(cm, x[j]);
+  float acc = 0.f;
+  if (cm > m) {
+    if (m != -INFINITY) s *= fast_exp2((m - cm) * kLog2e);
+    m = cm;
+  }
+  if (m == -INFINITY) {
+    // every value so far is -inf (contributes 0) unless one is NaN
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+      if (x[j] != x[j]) s = x[j];
+    return;
+  }
+  // x - m is exact for bf16 inputs; scaling afterwards keeps the rounding relative to the
+  // (small) shifted value instead of adding an absolute rounding of m * log2(e) to every term
+#pragma unroll
+  for (int j = 0; j < N; ++j) acc += fast_exp2((x[j] - m) * kLog2e);
+  s += acc;
+}
+
+__device__ __forceinline__ void warp_ms(float& m, float& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    ms_merge(m, s, m2, s2);
+  }
+}
+
+// Race winner: larger key wins, equal keys go to the lower index; idx < 0 means "none".
+__device__ __forceinline__ bool race_better(float k2, int32_t i2, float k1, int32_t i1) {
+  if (i2 < 0) return false;
+  if (i1 < 0) return true;
+  return k2 > k1 || (k2 == k1 && i2 < i1);
+}
+
+__device__ __forceinline__ void warp_race(float& key, int32_t& idx) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float k2 = __shfl_xor_sync(0xffffffffu, key, o);
+    const int32_t i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    if (race_better(k2, i2, key, idx)) {
+      key = k2;
+      idx = i2;
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace sv

@@ -1,0 +1,27 @@
+// sv_host.h -- host-side helpers shared by the entry points (argument checks, device queries).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "specverify.h"
+
+namespace sv {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+inline int elem_bytes(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
+
+// Number of SMs of the current device (queried once per device).
+int device_sm_count();
+
+// Resident CTAs per SM of `kernel` with `smem` bytes of dynamic shared memory (0 on error).
+int resident_ctas(const void* kernel, int threads, size_t smem);
+
+inline sv_status launch_status(cudaError_t e) {
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+}  // namespace sv

@@ -1,0 +1,174 @@
+"""GPU parity of spec_verify_token / spec_verify_block / spec_sample_draft with the CPU oracle.
+
+Every case feeds both sides the same seeded synthetic logits (synth) and the same drafted tokens
+(sampled from q by the oracle); the CUDA path is reached through the C ABI (ctypes binding)."""
+import numpy as np
+import pytest
+import torch
+
+from parity import compare_verify, host_f32, layout_np, oracle_tokens, oracle_verify
+from speculative_decoding_verification_token_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import speculative_decoding_verification_token_gb300 as sv
+    from speculative_decoding_verification_token_gb300 import build
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    return sv
+
+
+def _to_dev(inp):
+    d = dict(inp)
+    for k in ("target", "draft", "target_row0", "draft_row0", "draft_len"):
+        d[k] = inp[k].cuda()
+    return d
+
+
+def _run(sv, block, inp, tokens, request_ids=None):
+    fn = sv.spec_verify_block if block else sv.spec_verify_token
+    out = fn(inp["target"], inp["draft"], inp["target_row0"], inp["draft_row0"],
+             inp["draft_len"], inp["max_draft_len"], torch.from_numpy(tokens).cuda(),
+             inp["seed"], request_ids=request_ids)
+    torch.cuda.synchronize()
+    assert int(out["status"].item()) == 0, sv.status_string(int(out["status"].item()))
+    return out
+
+
+def _parity(sv, orc, block, inp, tokens=None, request_ids=None):
+    if tokens is None:
+        tokens = oracle_tokens(orc, inp)
+    rid_np = None if request_ids is None else request_ids.cpu().numpy()
+    ref = oracle_verify(orc, block, inp, tokens, request_ids=rid_np)
+    assert ref["status"] == 0
+    gpu = _run(sv, block, inp, tokens, request_ids)
+    lay = layout_np(inp)
+    res = compare_verify(gpu, ref, block, lay["draft_len"], lay["draft_row0"])
+    print(f"\n[parity] block={block} B={inp['B']} V={inp['V']}: {res}")
+    return gpu, ref, res
+
+
+@pytest.mark.parametrize("block", [0, 1])
+def test_token_small_workload(sv, orc, block):
+    """4 requests x 4 drafted positions, V = 1024, fp32, Philox seed 0."""
+    inp = _to_dev(synth.token_inputs(synth.TOKEN_SMALL, device="cpu"))
+    _parity(sv, orc, block, inp)
+
+
+@pytest.mark.parametrize("block", [0, 1])
+@pytest.mark.parametrize("V", [40000, 40003, 8191, 7])
+def test_scaled_bf16_ragged_vocab(sv, orc, block, V):
+    """bf16 rows spanning several 16 KB slices with a ragged tail (V not a multiple of 8 uses a
+    padded row stride)."""
+    w = synth.scaled(synth.TOKEN_LARGE, B=12, V=V)
+    inp = synth.token_inputs(w, device="cpu")
+    ld = (V + 7) // 8 * 8
+    for k in ("target", "draft"):
+        buf = torch.zeros((inp[k].shape[0], ld), dtype=inp[k].dtype)
+        buf[:, :V] = inp[k]
+        inp[k] = buf
+    inp = _to_dev(inp)
+    inp["target"] = inp["target"][:, :V]
+    inp["draft"] = inp["draft"][:, :V]
+    _parity(sv, orc, block, inp)
+
+
+@pytest.mark.parametrize("block", [0, 1])
+def test_ragged_lengths_and_scattered_rows(sv, orc, block):
+    """Per-request drafted lengths 0..7 and rows of each request placed out of order."""
+    w = synth.scaled(synth.BLOCK_LARGE, B=40, V=20000)
+    lens = synth.ragged_lengths(40, 7, seed=3)
+    inp = synth.token_inputs(w, device="cpu", draft_len=lens)
+    perm = torch.from_numpy(np.random.default_rng(4).permutation(40))
+    inp["target_row0"] = inp["target_row0"][perm].contiguous()
+    inp["draft_row0"] = inp["draft_row0"][perm].contiguous()
+    inp = _to_dev(inp)
+    rids = torch.from_numpy(np.random.default_rng(5).integers(0, 2**60, 40).astype(np.uint64)
+                            .view(np.int64)).cuda()
+    _parity(sv, orc, block, inp, request_ids=rids)
+
+
+@pytest.mark.parametrize("block", [0, 1])
+def test_full_size_workloads(sv, orc, block):
+    """Token-level: 64 requests x 5 positions, V = 151936 bf16.  Block: 128 requests x 7
+    positions, V = 129280 bf16.  Every request compared."""
+    w = synth.BLOCK_LARGE if block else synth.TOKEN_LARGE
+    inp = _to_dev(synth.token_inputs(w, device="cpu"))
+    _parity(sv, orc, block, inp)
+
+
+def test_sampler_matches_oracle(sv, orc):
+    """Draft tokens raced from q on the GPU equal the oracle's, except counted near-ties."""
+    for w in (synth.TOKEN_SMALL, synth.scaled(synth.TOKEN_LARGE, B=16, V=50000)):
+        inp = synth.token_inputs(w, device="cpu")
+        ref = oracle_tokens(orc, inp)
+        d = _to_dev(inp)
+        got = sv.spec_sample_draft(d["draft"], d["draft_row0"], d["draft_len"],
+                                   d["max_draft_len"], d["seed"]).cpu().numpy()
+        assert (got == ref).mean() > 0.99
+        # every mismatch must be a near-tie of the oracle's race
+        draft = host_f32(inp["draft"])
+        for row in np.flatnonzero(got != ref):
+            r, i = divmod(int(row), w.gamma)
+            st, tok, margin = orc.sample_race(draft[row], w.seed, r, i + 1, orc.TAG_DRAFT)
+            assert tok == ref[row] and margin < 1e-5
+
+
+def test_determinism(sv, orc):
+    inp = _to_dev(synth.token_inputs(synth.scaled(synth.TOKEN_LARGE, B=8, V=30000), "cpu"))
+    tokens = oracle_tokens(orc, inp)
+    a = _run(sv, 0, inp, tokens)
+    b = _run(sv, 0, inp, tokens)
+    assert torch.equal(a["out_tokens"], b["out_tokens"])
+    assert torch.equal(a["accept_ratio"], b["accept_ratio"])
+
+
+def test_all_zero_drafts_and_masked_rows(sv, orc):
+    """gamma = 0 everywhere (bonus only) and rows with masked (-inf) entries."""
+    w = synth.scaled(synth.TOKEN_LARGE, B=6, V=9000)
+    inp = synth.token_inputs(w, "cpu", draft_len=np.zeros(6, np.int32))
+    inp["target"][:, :4000] = float("-inf")
+    inp = _to_dev(inp)
+    gpu, ref, _ = _parity(sv, orc, 0, inp, tokens=np.zeros(inp["draft"].shape[0], np.int32))
+    assert (gpu["correction"].cpu().numpy() >= 4000).all()
+
+
+def test_data_errors_reported(sv, orc):
+    w = synth.scaled(synth.TOKEN_SMALL, B=2)
+    base = synth.token_inputs(w, "cpu")
+    tokens = oracle_tokens(orc, base)
+    cases = []
+    bad_tok = tokens.copy()
+    bad_tok[1] = w.V + 3
+    cases.append((base, bad_tok))
+    nan_in = dict(base, target=base["target"].clone())
+    nan_in["target"][2, 5] = float("nan")
+    cases.append((nan_in, tokens))
+    zq = dict(base, draft=base["draft"].clone())
+    zq["draft"][0, int(tokens[0])] = float("-inf")
+    cases.append((zq, tokens))
+    bad_len = dict(base, draft_len=torch.tensor([2, w.gamma + 1], dtype=torch.int32))
+    cases.append((bad_len, tokens))
+    for inp, toks in cases:
+        d = _to_dev(inp)
+        out = sv.spec_verify_token(d["target"], d["draft"], d["target_row0"], d["draft_row0"],
+                                   d["draft_len"], d["max_draft_len"],
+                                   torch.from_numpy(toks).cuda(), d["seed"])
+        torch.cuda.synchronize()
+        assert int(out["status"].item()) == sv.SV_ERR_BAD_INPUT
+
+
+def test_empty_batch_and_argument_errors(sv):
+    z = torch.zeros((1, 1024), device="cuda")
+    i64 = torch.zeros(0, dtype=torch.int64, device="cuda")
+    i32 = torch.zeros(0, dtype=torch.int32, device="cuda")
+    out = sv.spec_verify_token(z, z, i64, i64, i32, 4, torch.zeros(1, dtype=torch.int32,
+                                                                    device="cuda"), 0)
+    assert out["accepted_len"].numel() == 0
+    with pytest.raises(sv.SpecVerifyError):
+        sv.spec_verify_token(z, z, i64, i64, i32, sv.SV_MAX_DRAFT_LEN + 1,
+                             torch.zeros(1, dtype=torch.int32, device="cuda"), 0)

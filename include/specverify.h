@@ -11,6 +11,8 @@
  *     synchronously during the call.  The library allocates no memory and keeps no state between
  *     calls.  Scratch memory is the caller's `workspace` (DEVICE, 256-byte aligned), sized by the
  *     matching *_workspace_bytes query; its contents need no initialisation and are clobbered.
+ *     (spec_verify_token_noalloc is the one exception: its scratch is a fixed array inside the
+ *     library.)
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are asynchronous: they
  *     return after launching; outputs are valid once the stream reaches that point.
  *   - Argument errors (bad sizes, NULL required pointers, misaligned rows, a too-small workspace)
@@ -139,6 +141,29 @@ sv_status spec_sample_draft(const void* draft_logits, sv_dtype dtype, int64_t V,
                             int32_t max_draft_len, int32_t B, uint64_t seed,
                             const uint64_t* request_ids, int32_t* draft_tokens, int32_t* status,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Token-level verification that allocates nothing and takes no workspace (the pages have no
+ * counterpart: this is a packaging variant of spec_verify_token for callers that cannot allocate
+ * device memory, e.g. a plugin handed only its input and output buffers by an engine that owns all
+ * device memory, or a serving loop that must not call cudaMalloc because it can synchronise the
+ * device).  Arguments, results and data-error reporting are those of spec_verify_token.
+ * Scratch memory is a fixed array of SV_NOALLOC_SCRATCH_BYTES inside the library, held by every
+ * GPU that loads the library until the process exits; calls whose
+ * spec_verify_workspace_bytes(B, max_draft_len, V, dtype) exceeds it return SV_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  Every call shares the one
+ * array and clears the counters it needs before use, so calls that overlap on the GPU (other
+ * streams or other host threads) race on it and produce undefined results. */
+#define SV_NOALLOC_SCRATCH_BYTES (8u << 20)
+sv_status spec_verify_token_noalloc(const void* target_logits, const void* draft_logits,
+                                    sv_dtype dtype, int64_t V, int64_t ld,
+                                    const int64_t* target_row0, const int64_t* draft_row0,
+                                    const int32_t* draft_len, int32_t max_draft_len,
+                                    const int32_t* draft_tokens, int32_t B, uint64_t seed,
+                                    const uint64_t* request_ids, int32_t* accepted_len,
+                                    int32_t* out_tokens, int64_t out_ld,
+                                    int32_t* correction_token, float* accept_ratio,
+                                    int32_t* status, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * DSpark draft side.

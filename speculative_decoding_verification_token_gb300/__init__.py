@@ -60,6 +60,7 @@ def lib():
             "spec_verify_workspace_bytes": (sz, [i32, i32, i64, st]),
             "spec_verify_token": (st, verify_args + [P, P, P, sz, P]),
             "spec_verify_block": (st, verify_args + [P, P, P, P, sz, P]),
+            "spec_verify_token_noalloc": (st, verify_args + [P, P, P]),
             "spec_sample_draft": (st, [P, st, i64, i64, P, P, i32, i32, u64, P, P, P, P, sz, P]),
             "dspark_markov_workspace_bytes": (sz, [i32, i32, i64, i32]),
             "dspark_markov_draft": (st, [P, i64, P, P, i64, P, P, P, i32, i32, i64, i32, u64, P,

@@ -17,6 +17,7 @@
 // rejection, and therefore the correction race, most often falls -- are the most recently read
 // when the final kernel reads them again.
 #include <algorithm>
+#include <mutex>
 
 #include "sv_device.cuh"
 #include "sv_host.h"
@@ -1083,4 +1084,60 @@ extern "C" sv_status spec_sample_draft(const void* draft_logits, sv_dtype dtype,
     return run_sample<bf16_tag>(a, draft_row0, draft_len, seed, request_ids, draft_tokens, status,
                                 s);
   return run_sample<float>(a, draft_row0, draft_len, seed, request_ids, draft_tokens, status, s);
+}
+
+// ---------------------------------------------------------------------------------------------
+// spec_verify_token_noalloc: token-level verification with scratch memory owned by the library.
+//
+// Some callers cannot allocate device memory at all: a plugin that is handed only its input and
+// output buffers by a host engine that owns every device allocation, or a serving loop that must
+// not call cudaMalloc because a device allocation can implicitly synchronise the device.  For
+// them the scratch memory of the verify kernels lives in the file-scope array below, which every
+// GPU that loads this library holds until the process exits.
+// ---------------------------------------------------------------------------------------------
+namespace sv {
+
+constexpr size_t kNoAllocScratchBytes = SV_NOALLOC_SCRATCH_BYTES;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device.  In host code the array's name is a
+// host-side stand-in, not a device address, so the address is looked up once per device (with
+// that device current) and cached.
+static sv_status noalloc_scratch_address(void** out) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return SV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return SV_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return SV_OK;
+}
+
+}  // namespace sv
+
+extern "C" sv_status spec_verify_token_noalloc(
+    const void* target_logits, const void* draft_logits, sv_dtype dtype, int64_t V, int64_t ld,
+    const int64_t* target_row0, const int64_t* draft_row0, const int32_t* draft_len,
+    int32_t max_draft_len, const int32_t* draft_tokens, int32_t B, uint64_t seed,
+    const uint64_t* request_ids, int32_t* accepted_len, int32_t* out_tokens, int64_t out_ld,
+    int32_t* correction_token, float* accept_ratio, int32_t* status, void* stream) {
+  const size_t need = spec_verify_workspace_bytes(B, max_draft_len, V, dtype);
+  if (need == 0) return SV_ERR_INVALID;
+  if (need > sv::kNoAllocScratchBytes) return SV_ERR_UNSUPPORTED;  // batch too large for it
+  void* scratch = nullptr;
+  const sv_status st = sv::noalloc_scratch_address(&scratch);
+  if (st != SV_OK) return st;
+  // The plan kernel clears every counter of the scratch before the other kernels use it.
+  return spec_verify_token(target_logits, draft_logits, dtype, V, ld, target_row0, draft_row0,
+                           draft_len, max_draft_len, draft_tokens, B, seed, request_ids,
+                           accepted_len, out_tokens, out_ld, correction_token, accept_ratio,
+                           status, scratch, sv::kNoAllocScratchBytes, stream);
 }

@@ -75,6 +75,15 @@ const char* sv_status_string(sv_status status);
 /* Library build identifier (static string), e.g. for logs. */
 const char* sv_version(void);
 
+/* Kernel timing (diagnostic, off by default).  While enabled on the calling host thread, every
+ * spec_verify_token / spec_verify_block call records CUDA events on its stream around each of its
+ * kernels: [0] row streaming (all passes), [1] acceptance decisions, [2] correction / bonus race.
+ * sv_profile_read waits for the events of the last profiled call and returns the three durations
+ * in milliseconds.  The events belong to the library (created on first use, one set per host
+ * thread); nothing is recorded while profiling is disabled. */
+sv_status sv_profile_enable(int enable);
+sv_status sv_profile_read(float* ms_out /* HOST [3] */);
+
 /* ---------------------------------------------------------------------------------------------
  * Verification.
  *

@@ -57,6 +57,8 @@ def lib():
         sigs = {
             "sv_status_string": (C.c_char_p, [st]),
             "sv_version": (C.c_char_p, []),
+            "sv_profile_enable": (st, [C.c_int]),
+            "sv_profile_read": (st, [P]),
             "spec_verify_workspace_bytes": (sz, [i32, i32, i64, st]),
             "spec_verify_token": (st, verify_args + [P, P, P, sz, P]),
             "spec_verify_block": (st, verify_args + [P, P, P, P, sz, P]),
@@ -82,6 +84,17 @@ def status_string(code):
 
 def version():
     return lib().sv_version().decode()
+
+
+def sv_profile_enable(enable=True):
+    _check(lib().sv_profile_enable(int(enable)), "sv_profile_enable")
+
+
+def sv_profile_read():
+    """Durations (ms) of the last profiled verify call: [streaming, decisions, race]."""
+    out = (C.c_float * 3)()
+    _check(lib().sv_profile_read(out), "sv_profile_read")
+    return [float(x) for x in out]
 
 
 def _check(code, where):

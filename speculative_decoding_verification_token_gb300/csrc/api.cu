@@ -30,7 +30,41 @@ int resident_ctas(const void* kernel, int threads, size_t smem) {
   return n;
 }
 
+namespace {
+struct ProfileState {
+  bool enabled = false;
+  bool created = false;
+  cudaEvent_t ev[4];
+};
+thread_local ProfileState g_prof;
+}  // namespace
+
+void profile_mark(int k, cudaStream_t stream) {
+  if (!g_prof.enabled || !g_prof.created) return;
+  cudaEventRecord(g_prof.ev[k], stream);
+}
+
 }  // namespace sv
+
+extern "C" sv_status sv_profile_enable(int enable) {
+  sv::ProfileState& ps = sv::g_prof;
+  if (enable && !ps.created) {
+    for (int k = 0; k < 4; ++k)
+      if (cudaEventCreate(&ps.ev[k]) != cudaSuccess) return SV_ERR_CUDA;
+    ps.created = true;
+  }
+  ps.enabled = enable != 0;
+  return SV_OK;
+}
+
+extern "C" sv_status sv_profile_read(float* ms_out) {
+  sv::ProfileState& ps = sv::g_prof;
+  if (!ms_out || !ps.created) return SV_ERR_INVALID;
+  if (cudaEventSynchronize(ps.ev[3]) != cudaSuccess) return SV_ERR_CUDA;
+  for (int k = 0; k < 3; ++k)
+    if (cudaEventElapsedTime(&ms_out[k], ps.ev[k], ps.ev[k + 1]) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_OK;
+}
 
 extern "C" const char* sv_status_string(sv_status status) {
   switch (status) {

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "specverify.h"
@@ -249,6 +250,69 @@ __device__ __forceinline__ void warp_ms(float& m, float& s) {
     const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
     ms_merge(m, s, m2, s2);
   }
+}
+
+// ---- softmax statistics in the log2 domain: (m, s) with m a binary32 multiple of the row maximum
+// times log2(e) and s = sum 2^(x log2(e) - m).  fma(x, log2e, -m) rounds once, relative to the
+// (small) shifted value, so the reference point 2^m is exact and carries no rounding into the sum.
+// m starts at kM2Empty (finite, below every real value): an all -inf stretch keeps s = 0 and a NaN
+// or +inf logit turns s into NaN, which the combining step reports.
+constexpr float kM2Empty = -1.0e30f;
+
+__device__ __forceinline__ void ms2_merge(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  s = s * fast_exp2(m - mn) + s2 * fast_exp2(m2 - mn);
+  m = mn;
+}
+
+// Warp-wide (m, s): the common maximum first, then one rescale per lane and a plain sum.
+__device__ __forceinline__ void warp_ms2(float& m, float& s) {
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  s *= fast_exp2(m - M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  m = M;
+}
+
+// Fold one 16-byte vector of logits into (m, s): the vector maximum decides a (rare) rescale,
+// then every element costs one fma, one ex2 and one add (summed as a tree).
+__device__ __forceinline__ void ms2_fold(float& m, float& s, const float* x, float vmax, int n) {
+  const float vm = vmax * kLog2e;
+  if (vm > m) {
+    s *= fast_exp2(m - vm);
+    m = vm;
+  }
+  float e[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) e[j] = j < n ? fast_exp2(fmaf(x[j], kLog2e, -m)) : 0.f;
+  s += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+}
+
+__device__ __forceinline__ void ms2_vec_bf16(float& m, float& s, const uint4& v) {
+  __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.x),
+                             *reinterpret_cast<const __nv_bfloat162*>(&v.y));
+  const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.z),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&v.w));
+  a = __hmax2(a, b);
+  const uint32_t ab = *reinterpret_cast<const uint32_t*>(&a);
+  const float vmax = fmaxf(__uint_as_float(ab << 16), __uint_as_float(ab & 0xFFFF0000u));
+  float x[8];
+  Elem<bf16_tag>::unpack(v, x);
+  ms2_fold(m, s, x, vmax, 8);
+}
+
+__device__ __forceinline__ void ms2_vec_f32(float& m, float& s, const uint4& v) {
+  float x[8];
+  Elem<float>::unpack(v, x);
+  const float vmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  ms2_fold(m, s, x, vmax, 4);
+}
+
+__device__ __forceinline__ void ms2_one(float& m, float& s, float x) {
+  float xs[8] = {x, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  ms2_fold(m, s, xs, x, 1);
 }
 
 // Race winner: larger key wins, equal keys go to the lower index; idx < 0 means "none".

@@ -20,6 +20,9 @@ int device_sm_count();
 // Resident CTAs per SM of `kernel` with `smem` bytes of dynamic shared memory (0 on error).
 int resident_ctas(const void* kernel, int threads, size_t smem);
 
+// Diagnostic kernel timing (sv_profile_enable): record event `k` (0..3) on `stream` if enabled.
+void profile_mark(int k, cudaStream_t stream);
+
 inline sv_status launch_status(cudaError_t e) {
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -187,15 +187,21 @@ size_t dspark_markov_workspace_bytes(int32_t B, int32_t K, int64_t V, int32_t R)
  *   x_k = argmax_v z_k(v) - log(-log u_v)           (DRAFT tag, position k)
  *   conf_k = 1 / (1 + exp(-conf_scores[b][k] / sts_T[k]))   (sequential temperature scaling)
  * backbone_logits: DEVICE bf16 [B][K][V], row (b, k) at (b * K + k) * ldb elements;
- * U: DEVICE bf16 [V][R] (row stride R); W: DEVICE bf16 [R][V] (row stride ldw);
+ * U: DEVICE bf16 [V][R] (row stride R); Wt: DEVICE bf16 [V][R], the factor W [R][V] stored
+ * transposed (Wt[v][j] = W[j][v], row stride ldw >= R) so that both GEMM operands are K-major;
  * anchor_token: DEVICE int32 [B]; conf_scores: DEVICE fp32 [B][K]; sts_T: DEVICE fp32 [K].
  * R must be 256 (SV_ERR_UNSUPPORTED otherwise); 1 <= K <= SV_MAX_DRAFT_LEN.
  * Outputs: draft_tokens DEVICE int32 [B][K]; draft_logits_out (nullable) DEVICE bf16 [B][K][V]
  * with row stride ldz -- the exact rows the tokens were sampled from, to be passed to verify;
  * row_stats (nullable) fp32 [B][K][2] = (max z, log-sum-exp z); conf_out (nullable) fp32 [B][K].
- * request_ids as for verify.  ldb, ldw, ldz: multiples of 8 elements. */
+ * request_ids as for verify.  ldb, ldw, ldz: multiples of 8 elements; backbone_logits, U, Wt
+ * and draft_logits_out 16-byte aligned; workspace 256-byte aligned, at least
+ * dspark_markov_workspace_bytes(B, K, V, R) bytes, owned by the caller and free again once the
+ * stream has passed this call.  conf_out needs conf_scores and sts_T.  An out-of-range anchor or
+ * a row of z without a finite maximum (or holding NaN / +inf) writes SV_ERR_BAD_INPUT to status
+ * and drafts token 0 there.  All work is queued on `stream`; nothing is allocated. */
 sv_status dspark_markov_draft(const void* backbone_logits, int64_t ldb, const void* U,
-                              const void* W, int64_t ldw, const int32_t* anchor_token,
+                              const void* Wt, int64_t ldw, const int32_t* anchor_token,
                               const float* conf_scores, const float* sts_T, int32_t B, int32_t K,
                               int64_t V, int32_t R, uint64_t seed, const uint64_t* request_ids,
                               int32_t* draft_tokens, void* draft_logits_out, int64_t ldz,

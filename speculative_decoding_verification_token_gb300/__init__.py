@@ -119,8 +119,9 @@ def _dtype_code(t):
     raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
 
 
-def _dev(t, dtype=None, rows=False):
-    """Checks a device tensor; `rows` allows a row-strided 2-D view (logits with ld > V)."""
+def _dev(t, dtype=None, rows=False, strided=False):
+    """Checks a device tensor; `rows` allows a row-strided 2-D view (logits with ld > V) and
+    `strided` leaves the layout to the caller's own checks."""
     if t is None:
         return None
     if not t.is_cuda:
@@ -130,7 +131,7 @@ def _dev(t, dtype=None, rows=False):
     if rows:
         if t.dim() != 2 or t.stride(1) != 1:
             raise ValueError("logits must be a 2-D tensor with unit column stride")
-    elif not t.is_contiguous():
+    elif not strided and not t.is_contiguous():
         raise ValueError("tensors passed to the library must be contiguous")
     return t
 
@@ -248,27 +249,38 @@ def dspark_markov_workspace_bytes(B, K, V, R):
     return int(lib().dspark_markov_workspace_bytes(B, K, V, R))
 
 
-def dspark_markov_draft(backbone, U, W, anchor, conf_scores, sts_T, seed, request_ids=None,
+def dspark_markov_draft(backbone, U, Wt, anchor, conf_scores, sts_T, seed, request_ids=None,
                         want_logits=True, want_stats=True, status=None, workspace=None,
                         stream=None):
-    """Markov-head drafting.  backbone bf16 [B, K, V]; U bf16 [V, R]; W bf16 [R, V]."""
-    _dev(backbone, torch.bfloat16), _dev(U, torch.bfloat16), _dev(W, torch.bfloat16)
-    _dev(anchor, torch.int32), _dev(conf_scores, torch.float32), _dev(sts_T, torch.float32)
+    """Markov-head drafting.  backbone bf16 [B, K, V] (rows may be padded: stride(1) = ldb,
+    stride(0) = K * ldb); U bf16 [V, R]; Wt bf16 [V, R] (W stored transposed, rows may be padded);
+    anchor int32 [B]; conf_scores fp32 [B, K] and sts_T fp32 [K], or both None (no confidence)."""
+    _dev(backbone, torch.bfloat16, strided=True), _dev(U, torch.bfloat16)
+    _dev(Wt, torch.bfloat16, strided=True), _dev(anchor, torch.int32)
+    if conf_scores is not None:
+        _dev(conf_scores, torch.float32), _dev(sts_T, torch.float32)
     B, K, V = backbone.shape
     R = U.shape[1]
+    ldb = backbone.stride(1)
+    if backbone.stride(2) != 1 or backbone.stride(0) != K * ldb:
+        raise ValueError("backbone must be [B, K, V] with unit column stride and rows ldb apart")
+    if U.stride(1) != 1 or U.stride(0) != R or Wt.stride(1) != 1 or Wt.shape[0] != V:
+        raise ValueError("U must be a contiguous [V, R] tensor and Wt a [V, R] row-major tensor")
     dev = backbone.device
     tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
-    z = torch.empty((B, K, V), dtype=torch.bfloat16, device=dev) if want_logits else None
+    ldz = (V + 7) // 8 * 8  # rows of z start on 16-byte boundaries
+    z = (torch.empty((B, K, ldz), dtype=torch.bfloat16, device=dev)[:, :, :V] if want_logits
+         else None)
     stats = torch.empty((B, K, 2), dtype=torch.float32, device=dev) if want_stats else None
-    conf = torch.empty((B, K), dtype=torch.float32, device=dev)
+    conf = torch.empty((B, K), dtype=torch.float32, device=dev) if conf_scores is not None else None
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
     need = dspark_markov_workspace_bytes(B, K, V, R)
     ws = workspace if workspace is not None else globals()["workspace"](need, dev)
-    code = lib().dspark_markov_draft(_ptr(backbone), V, _ptr(U), _ptr(W), W.stride(0),
+    code = lib().dspark_markov_draft(_ptr(backbone), ldb, _ptr(U), _ptr(Wt), Wt.stride(0),
                                      _ptr(anchor), _ptr(conf_scores), _ptr(sts_T), B, K, V, R,
                                      int(seed), _ptr(request_ids), _ptr(tokens), _ptr(z),
-                                     V, _ptr(stats), _ptr(conf), _ptr(status), _ptr(ws),
+                                     ldz, _ptr(stats), _ptr(conf), _ptr(status), _ptr(ws),
                                      ws.numel(), _stream(stream))
     _check(code, "dspark_markov_draft")
     return {"draft_tokens": tokens, "draft_logits": z, "row_stats": stats, "conf": conf,

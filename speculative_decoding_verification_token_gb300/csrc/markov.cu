@@ -1,15 +1,503 @@
-// markov.cu -- DSpark Markov-head drafting (placeholder until the tcgen05 kernel lands).
-#include "sv_host.h"
+// markov.cu -- DSpark Markov-head drafting (dspark_markov_draft).
+//
+// For every draft position k = 1..K (left to right, because row k depends on the token sampled at
+// k - 1) two kernels run on the caller's stream:
+//   position  persistent, warp-specialised CTAs, each owning a 128-request block and a strided
+//             set of 64-column vocabulary tiles.  The CTA gathers the 128 rows U[x_{k-1}] (the
+//             GEMM's A operand, 64 KB, kept in shared memory for every tile) and then pipelines:
+//               warp 0      tensor-TMA loads of the Wt tile (64 vocabulary rows x 256) and of the
+//                           backbone tile (128 requests x 64 columns) into a two-stage ring;
+//               warp 1      tcgen05.mma (M = 128, N = 64, K = 256) into one of two TMEM
+//                           accumulators;
+//               warps 2-9   the epilogue: TMEM -> registers, + backbone, round to bf16, TMA store
+//                           of z, and per request: log2-domain softmax statistics and the
+//                           exponential race x_k = argmax z - log(-log u) (DRAFT tag, position k)
+//                           with the noise gate, written as one partial per (request, CTA).
+//   select    folds the partials of every request into x_k, the row statistics of z_k and the
+//             sequential-temperature-scaled confidence conf_k = 1 / (1 + exp(-s_k / T_k)).
+#include <algorithm>
+#include <cstring>
+#include <mutex>
 
-extern "C" size_t dspark_markov_workspace_bytes(int32_t B, int32_t K, int64_t V, int32_t R) {
-  (void)B; (void)K; (void)V; (void)R;
-  return 256;
+#include "race.cuh"
+#include "sv_device.cuh"
+#include "sv_host.h"
+#include "tc.cuh"
+
+namespace sv {
+
+constexpr int kMkRows = 128;                 // requests per M-block (UMMA M)
+constexpr int kMkCols = 64;                  // vocabulary columns per tile (UMMA N)
+constexpr int kMkRank = 256;                 // R (UMMA K)
+constexpr int kMkKB = kMkRank / 64;          // 128-byte k-blocks per row
+constexpr int kMkStages = 2;                 // Wt / backbone ring depth
+constexpr int kMkEpiWarps = 8;
+constexpr int kMkThreads = 32 * (2 + kMkEpiWarps);
+constexpr uint32_t kMkABytes = kMkKB * kMkRows * 128;     // 64 KB
+constexpr uint32_t kMkBBytes = kMkKB * kMkCols * 128;     // 32 KB per stage
+constexpr uint32_t kMkBBBytes = kMkRows * 128;            // 16 KB per stage (64 bf16 per row)
+constexpr uint32_t kMkZBytes = kMkRows * 128;             // 16 KB per z staging buffer
+constexpr size_t kMkSmem = 1024 + kMkABytes + kMkStages * (kMkBBytes + kMkBBBytes) + 2 * kMkZBytes;
+constexpr uint32_t kMkTmemCols = 2 * kMkCols;             // two accumulators
+
+struct MkPartial {  // one (request, CTA) partial of position k
+  float m2;         // log2-domain running maximum
+  float s;          // sum of 2^(z log2e - m2)
+  float zmax;       // largest z
+  float key;        // best race key
+  int32_t idx;      // its vocabulary index
+  int32_t pad[3];
+};
+
+struct MkParams {
+  const void* U;              // bf16 [V][R]
+  const int32_t* anchor;      // [B]
+  int32_t* tokens;            // [B][K] drafted tokens (x_{k-1} read from here for k > 1)
+  int32_t B, K, k;            // k: 1-based position
+  int64_t V;
+  int32_t n_mblocks, per_mblock, n_tiles;
+  uint64_t seed;
+  const uint64_t* request_ids;
+  int32_t write_z;
+  MkPartial* partials;        // [B][per_mblock]
+  int32_t* status;
+};
+
+__device__ __forceinline__ float bf16_round_f(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
 }
 
-extern "C" sv_status dspark_markov_draft(const void*, int64_t, const void*, const void*, int64_t,
-                                         const int32_t*, const float*, const float*, int32_t,
-                                         int32_t, int64_t, int32_t, uint64_t, const uint64_t*,
-                                         int32_t*, void*, int64_t, float*, float*, int32_t*, void*,
-                                         size_t, void*) {
-  return SV_ERR_UNSUPPORTED;
+template <int kDummy = 0>
+__global__ void __launch_bounds__(kMkThreads, 1)
+    markov_position_kernel(const __grid_constant__ CUtensorMap map_wt,
+                           const __grid_constant__ CUtensorMap map_bb,
+                           const __grid_constant__ CUtensorMap map_z, MkParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + kMkABytes;                          // [stage][kb] 8 KB tiles
+  uint8_t* sBB = sB + kMkStages * kMkBBytes;             // [stage] 16 KB
+  uint8_t* sZ = sBB + kMkStages * kMkBBBytes;            // [2] 16 KB
+  __shared__ uint64_t b_full[kMkStages], b_empty[kMkStages];
+  __shared__ uint64_t bb_full[kMkStages], bb_empty[kMkStages];
+  __shared__ uint64_t acc_full[2], acc_empty[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ float merge[kMkRows][5];
+  __shared__ uint32_t gate[kGateBuckets];
+  __shared__ int32_t s_bad;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int32_t mb = blockIdx.x % p.n_mblocks;
+  const int32_t ci = blockIdx.x / p.n_mblocks;
+  const int32_t m0 = mb * kMkRows;
+  const int32_t n_my = ci < p.n_tiles ? (p.n_tiles - ci + p.per_mblock - 1) / p.per_mblock : 0;
+
+  if (tid == 0) {
+    s_bad = 0;
+    for (int s = 0; s < kMkStages; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
+      mbar_init(&bb_full[s], 1);
+      mbar_init(&bb_empty[s], kMkEpiWarps);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], kMkEpiWarps);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(&tmem_base, kMkTmemCols);
+  build_gate(gate);
+
+  // A operand: the 128 rows U[x_{k-1}] in the swizzled K-major layout (rows past B use row 0)
+  {
+    const uint8_t* U = static_cast<const uint8_t*>(p.U);
+    for (int c = tid; c < kMkRows * (kMkRank / 8); c += kMkThreads) {
+      const int r = c / (kMkRank / 8);       // tile row
+      const int ch = c % (kMkRank / 8);      // 16-byte chunk along K (0..31)
+      const int32_t b = m0 + r;
+      int32_t x = 0;
+      if (b < p.B) {
+        x = p.k == 1 ? p.anchor[b] : p.tokens[size_t(b) * p.K + (p.k - 2)];
+        if (x < 0 || int64_t(x) >= p.V) {
+          s_bad = 1;
+          x = 0;
+        }
+      }
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(U + size_t(x) * (kMkRank * 2)) + ch);
+      const int kb = ch >> 3;
+      *reinterpret_cast<uint4*>(sA + kb * (kMkRows * 128) + tc::sw128(r, ch & 7)) = v;
+    }
+  }
+  fence_proxy_async();  // the gathered rows are read by the tensor cores (async proxy)
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (tid == 0 && s_bad) report(p.status, SV_ERR_BAD_INPUT);
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0) {
+    // ---- producer
+    if (lane == 0) {
+      for (int t = 0; t < n_my; ++t) {
+        const int32_t n = ci + t * p.per_mblock;
+        const int s = t % kMkStages;
+        const uint32_t use = t / kMkStages;
+        if (t >= kMkStages && !mbar_wait(&b_empty[s], (use - 1) & 1, p.status)) break;
+        mbar_expect_tx(&b_full[s], kMkBBytes);
+        for (int kb = 0; kb < kMkKB; ++kb)
+          tc::tma_load_2d(sB + s * kMkBBytes + kb * (kMkCols * 128), &map_wt, kb * 64,
+                          n * kMkCols, &b_full[s]);
+        if (t >= kMkStages && !mbar_wait(&bb_empty[s], (use - 1) & 1, p.status)) break;
+        mbar_expect_tx(&bb_full[s], kMkBBBytes);
+        tc::tma_load_3d(sBB + s * kMkBBBytes, &map_bb, n * kMkCols, p.k - 1, m0, &bb_full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    // ---- tensor-core issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kMkRows, kMkCols);
+      const uint32_t a_base = smem_addr(sA);
+      for (int t = 0; t < n_my; ++t) {
+        const int s = t % kMkStages;
+        const int acc = t & 1;
+        if (t >= 2 && !mbar_wait(&acc_empty[acc], ((t >> 1) - 1) & 1, p.status)) break;
+        if (!mbar_wait(&b_full[s], (t / kMkStages) & 1, p.status)) break;
+        tc::fence_after_sync();
+        const uint32_t b_base = smem_addr(sB + s * kMkBBytes);
+        for (int kb = 0; kb < kMkKB; ++kb)
+          for (int ks = 0; ks < 4; ++ks)  // 16 K-elements (32 bytes) per instruction
+            tc::mma_bf16(tmem + acc * kMkCols,
+                         tc::smem_desc_sw128(a_base + kb * (kMkRows * 128) + ks * 32),
+                         tc::smem_desc_sw128(b_base + kb * (kMkCols * 128) + ks * 32), idesc,
+                         (kb | ks) != 0);
+        tc::mma_commit(&b_empty[s]);
+        tc::mma_commit(&acc_full[acc]);
+      }
+    }
+  } else {
+    // ---- epilogue: warp w reads TMEM lane quadrant q = w % 4 (rows 32q .. 32q + 31) and column
+    // half h of each 64-column tile; thread (q, lane) owns request m0 + 32q + lane.
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int r = 32 * q + lane;
+    const int32_t b = m0 + r;
+    const int etid = tid - 64;             // 0..255 among the epilogue threads
+    const bool issuer = etid == 0;         // issues the z stores
+    const uint64_t req = b < p.B ? (p.request_ids ? p.request_ids[b] : uint64_t(b)) : 0;
+    const Stream st = make_stream(p.seed, req, static_cast<uint32_t>(p.k), 0u /* DRAFT */);
+    float m2 = kM2Empty, s = 0.f, zmax = -INFINITY, best = -INFINITY;
+    int32_t best_idx = -1;
+    bool failed = false;
+    for (int t = 0; t < n_my; ++t) {
+      const int32_t n = ci + t * p.per_mblock;
+      const int sb = t % kMkStages;
+      const int acc = t & 1;
+      float v[32];
+      if (!failed && !mbar_wait(&acc_full[acc], (t >> 1) & 1, p.status)) failed = true;
+      __syncwarp();
+      tc::fence_after_sync();
+      tc::tmem_load32(tmem + (uint32_t(32 * q) << 16) + acc * kMkCols + h * 32, v);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (!failed && !mbar_wait(&bb_full[sb], (t / kMkStages) & 1, p.status)) failed = true;
+      uint4 bbv[4];
+      {
+        const uint8_t* tile = sBB + sb * kMkBBBytes;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          bbv[c] = *reinterpret_cast<const uint4*>(tile + tc::sw128(r, 4 * h + c));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bb_empty[sb]);
+      // z = bf16(acc + backbone); columns past V become -inf (they hold zero-filled operands)
+      const int64_t c0 = int64_t(n) * kMkCols + h * 32;
+      uint32_t zp[16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float bb[8];
+        Elem<bf16_tag>::unpack(bbv[c], bb);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          const __nv_bfloat162 z2 = __floats2bfloat162_rn(v[8 * c + j] + bb[j],
+                                                          v[8 * c + j + 1] + bb[j + 1]);
+          zp[4 * c + j / 2] = *reinterpret_cast<const uint32_t*>(&z2);
+          const float2 zf = __bfloat1622float2(z2);
+          v[8 * c + j] = c0 + 8 * c + j < p.V ? zf.x : -INFINITY;
+          v[8 * c + j + 1] = c0 + 8 * c + j + 1 < p.V ? zf.y : -INFINITY;
+        }
+      }
+      // softmax statistics (log2 domain) and the largest z
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float* x = v + 8 * c;
+        const float vmax = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
+                                 fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+        zmax = fmaxf(zmax, vmax);
+        ms2_fold(m2, s, x, vmax, 8);
+      }
+      // exponential race: entry e keys z_e - log(-log u_e); the noise gate against the running
+      // best key rejects most entries on the Philox word alone
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const uint4 blk = stream_block(st, static_cast<uint32_t>((c0 >> 2) + g));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float z = v[4 * g + j];
+          const uint32_t w = word_of(blk, j);
+          if (z > -INFINITY && gate_passes(gate, best, z, w)) {
+            const float key = z + race_noise(uniform_of(w));
+            const int32_t e = static_cast<int32_t>(c0 + 4 * g + j);
+            if (race_better(key, e, best, best_idx)) {
+              best = key;
+              best_idx = e;
+            }
+          }
+        }
+      }
+      if (p.write_z) {
+        // sZ[t & 1] is free once the store issued two tiles ago has read it
+        if (issuer) tc::bulk_wait_read<1>();
+        named_sync(1, 32 * kMkEpiWarps);
+        uint8_t* zt = sZ + (t & 1) * kMkZBytes;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(zt + tc::sw128(r, 4 * h + c)) =
+              make_uint4(zp[4 * c], zp[4 * c + 1], zp[4 * c + 2], zp[4 * c + 3]);
+        fence_proxy_async();
+        named_sync(1, 32 * kMkEpiWarps);
+        if (issuer) {
+          tc::tma_store_3d(&map_z, zt, n * kMkCols, p.k - 1, m0);
+          tc::bulk_commit();
+        }
+      }
+    }
+    // fold the two column halves of every request and publish this CTA's partial
+    if (h == 1) {
+      merge[r][0] = m2;
+      merge[r][1] = s;
+      merge[r][2] = zmax;
+      merge[r][3] = best;
+      merge[r][4] = __int_as_float(best_idx);
+    }
+    named_sync(1, 32 * kMkEpiWarps);
+    if (h == 0 && b < p.B) {
+      ms2_merge(m2, s, merge[r][0], merge[r][1]);
+      zmax = fmaxf(zmax, merge[r][2]);
+      const int32_t i2 = __float_as_int(merge[r][4]);
+      if (race_better(merge[r][3], i2, best, best_idx)) {
+        best = merge[r][3];
+        best_idx = i2;
+      }
+      MkPartial out;
+      out.m2 = m2;
+      out.s = s;
+      out.zmax = zmax;
+      out.key = best;
+      out.idx = best_idx;
+      out.pad[0] = out.pad[1] = out.pad[2] = 0;
+      p.partials[size_t(b) * p.per_mblock + ci] = out;
+    }
+    if (issuer) tc::bulk_wait_all();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kMkTmemCols);
+  }
+}
+
+// One warp per request: fold the CTA partials of position k into x_k, the statistics of z_k and
+// the confidence.  A row without a finite maximum or with a NaN / +inf entry reports BAD_INPUT
+// and drafts token 0 (so the next position still reads a valid row of U).
+__global__ void __launch_bounds__(256)
+    markov_select_kernel(const MkPartial* __restrict__ partials, int32_t per, int32_t B,
+                         int32_t K, int32_t k, const float* __restrict__ conf_scores,
+                         const float* __restrict__ sts_T, int32_t* tokens, float* row_stats,
+                         float* conf_out, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int32_t b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (b >= B) return;
+  float m2 = kM2Empty, s = 0.f, zmax = -INFINITY, key = -INFINITY;
+  int32_t idx = -1;
+  for (int32_t i = lane; i < per; i += 32) {
+    const MkPartial pt = partials[size_t(b) * per + i];
+    ms2_merge(m2, s, pt.m2, pt.s);
+    zmax = fmaxf(zmax, pt.zmax);
+    if (race_better(pt.key, pt.idx, key, idx)) {
+      key = pt.key;
+      idx = pt.idx;
+    }
+  }
+  warp_ms2(m2, s);
+  zmax = warp_max(zmax);
+  warp_race(key, idx);
+  if (lane == 0) {
+    const size_t o = size_t(b) * K + (k - 1);
+    const bool bad = idx < 0 || !(s > 0.f) || isinf(s) || !(zmax < INFINITY);
+    if (bad) report(status, SV_ERR_BAD_INPUT);
+    tokens[o] = bad ? 0 : idx;
+    if (row_stats) {
+      row_stats[2 * o] = zmax;
+      row_stats[2 * o + 1] = (m2 + log2f(s)) * kLn2;
+    }
+    if (conf_out) conf_out[o] = 1.f / (1.f + expf(-conf_scores[o] / sts_T[k - 1]));
+  }
+}
+
+// ---- host side --------------------------------------------------------------------------------
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims[0] is the contiguous one, strides in bytes for
+// dims 1.. ; out-of-range elements load as zero and are skipped by stores.
+bool make_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  cuuint64_t d[3], st[2];
+  cuuint32_t bx[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, bx, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct MkGeom {
+  int32_t n_mblocks, per_mblock, n_tiles;
+};
+
+// 128-request blocks x vocabulary tiles; one CTA per SM, the SMs split evenly between the blocks.
+bool markov_geom(int32_t B, int64_t V, MkGeom* g) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return false;
+  g->n_mblocks = (B + kMkRows - 1) / kMkRows;
+  g->n_tiles = static_cast<int32_t>((V + kMkCols - 1) / kMkCols);
+  g->per_mblock = std::max(1, std::min(sms / std::max(1, g->n_mblocks), g->n_tiles));
+  return true;
+}
+
+size_t markov_ws_bytes(int32_t B, const MkGeom& g) {
+  return (size_t(B) * g.per_mblock * sizeof(MkPartial) + 255) & ~size_t(255);
+}
+
+}  // namespace
+}  // namespace sv
+
+extern "C" size_t dspark_markov_workspace_bytes(int32_t B, int32_t K, int64_t V, int32_t R) {
+  (void)K;
+  (void)R;
+  sv::MkGeom g;
+  if (B <= 0 || V <= 0 || !sv::markov_geom(B, V, &g)) return 0;
+  return sv::markov_ws_bytes(B, g);
+}
+
+extern "C" sv_status dspark_markov_draft(const void* backbone_logits, int64_t ldb, const void* U,
+                                         const void* Wt, int64_t ldw,
+                                         const int32_t* anchor_token, const float* conf_scores,
+                                         const float* sts_T, int32_t B, int32_t K, int64_t V,
+                                         int32_t R, uint64_t seed, const uint64_t* request_ids,
+                                         int32_t* draft_tokens, void* draft_logits_out,
+                                         int64_t ldz, float* row_stats, float* conf_out,
+                                         int32_t* status, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  using namespace sv;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (B < 0 || K < 1 || K > SV_MAX_DRAFT_LEN || V < 1 || R < 1) return SV_ERR_INVALID;
+  if (R != kMkRank || V > (int64_t(1) << 31) - kMkCols) return SV_ERR_UNSUPPORTED;
+  if (!backbone_logits || !U || !Wt || !anchor_token || !draft_tokens) return SV_ERR_INVALID;
+  if (conf_out && (!conf_scores || !sts_T)) return SV_ERR_INVALID;
+  if (ldb < V || ldw < R || (draft_logits_out && ldz < V)) return SV_ERR_INVALID;
+  if (ldb % 8 || ldw % 8 || (draft_logits_out && ldz % 8)) return SV_ERR_UNSUPPORTED;
+  if (!aligned16(backbone_logits) || !aligned16(U) || !aligned16(Wt) ||
+      (draft_logits_out && !aligned16(draft_logits_out)))
+    return SV_ERR_UNSUPPORTED;
+  if (status && cudaMemsetAsync(status, 0, sizeof(int32_t), cs) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (B == 0) return SV_OK;
+  MkGeom g;
+  if (!markov_geom(B, V, &g)) return SV_ERR_CUDA;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < markov_ws_bytes(B, g))
+    return SV_ERR_INVALID;
+
+  // tensor maps: Wt [V][R]; backbone and z [B][K][V] with row (b, k) at (b K + k) ld elements
+  CUtensorMap map_wt, map_bb, map_z;
+  {
+    const uint64_t dims[2] = {uint64_t(R), uint64_t(V)};
+    const uint64_t strides[1] = {uint64_t(ldw) * 2};
+    const uint32_t box[2] = {64, kMkCols};
+    if (!make_map(&map_wt, Wt, 2, dims, strides, box)) return SV_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {uint64_t(V), uint64_t(K), uint64_t(B)};
+    const uint64_t strides[2] = {uint64_t(ldb) * 2, uint64_t(ldb) * 2 * K};
+    const uint32_t box[3] = {kMkCols, 1, kMkRows};
+    if (!make_map(&map_bb, backbone_logits, 3, dims, strides, box)) return SV_ERR_CUDA;
+  }
+  if (draft_logits_out) {
+    const uint64_t dims[3] = {uint64_t(V), uint64_t(K), uint64_t(B)};
+    const uint64_t strides[2] = {uint64_t(ldz) * 2, uint64_t(ldz) * 2 * K};
+    const uint32_t box[3] = {kMkCols, 1, kMkRows};
+    if (!make_map(&map_z, draft_logits_out, 3, dims, strides, box)) return SV_ERR_CUDA;
+  } else {
+    map_z = map_bb;  // never used: write_z = 0
+  }
+  if (cudaFuncSetAttribute(markov_position_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kMkSmem)) != cudaSuccess)
+    return SV_ERR_CUDA;
+
+  MkParams p;
+  p.U = U;
+  p.anchor = anchor_token;
+  p.tokens = draft_tokens;
+  p.B = B;
+  p.K = K;
+  p.V = V;
+  p.n_mblocks = g.n_mblocks;
+  p.per_mblock = g.per_mblock;
+  p.n_tiles = g.n_tiles;
+  p.seed = seed;
+  p.request_ids = request_ids;
+  p.write_z = draft_logits_out != nullptr;
+  p.partials = static_cast<MkPartial*>(workspace);
+  p.status = status;
+  const int grid = g.n_mblocks * g.per_mblock;
+  const int sel_grid = (B + 7) / 8;
+  profile_mark(0, cs);
+  for (int32_t k = 1; k <= K; ++k) {
+    p.k = k;
+    markov_position_kernel<0><<<grid, kMkThreads, kMkSmem, cs>>>(map_wt, map_bb, map_z, p);
+    if (k == 1) profile_mark(1, cs);
+    markov_select_kernel<<<sel_grid, 256, 0, cs>>>(p.partials, g.per_mblock, B, K, k, conf_scores,
+                                                   sts_T, draft_tokens, row_stats, conf_out,
+                                                   status);
+    if (k == 1) profile_mark(2, cs);
+  }
+  profile_mark(3, cs);
+  return launch_status(cudaGetLastError());
 }

@@ -125,10 +125,6 @@ struct StageMeta {
   float A, gap, mt, pad;  // residual pass: rho_{i-1} / s_t, gap, m_t (log2 units)
 };
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 template <typename E>
 __device__ void stream_producer(const StreamParams& p, uint8_t* ring, uint64_t* full,
                                 uint64_t* empty, StageMeta* meta) {

@@ -129,7 +129,11 @@ class MarkovWorkload:
     gen_seed: int
 
 
-MARKOV = MarkovWorkload("markov", 256, 16, 151936, 256, 2.0, 0.02, 3, 1004)
+# U, W entries ~ N(0, 0.25^2) make the rank-256 transition bias U[x] . W ~ N(0, 1): the bigram
+# term moves the logits by about as much as one backbone standard deviation.
+MARKOV = MarkovWorkload("markov", 256, 16, 151936, 256, 2.0, 0.25, 3, 1004)
+# several M-blocks and vocabulary tiles with ragged tails (B % 128 != 0, V % 64 != 0)
+MARKOV_SMALL = MarkovWorkload("markov_small", 200, 3, 1000, 256, 2.0, 0.25, 5, 1006)
 
 
 def markov_inputs(w: MarkovWorkload, device="cpu"):
@@ -145,6 +149,7 @@ def markov_inputs(w: MarkovWorkload, device="cpu"):
         "backbone": backbone.to(torch.bfloat16),
         "U": U.to(torch.bfloat16),
         "W": W.to(torch.bfloat16),
+        "Wt": W.t().contiguous().to(torch.bfloat16),
         "anchor": anchor.to(torch.int32),
         "scores": scores.float(),
         "T": T.float(),

@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import concurrent.futures as cf
+import dataclasses
 import hashlib
 import json
 import os
@@ -44,6 +45,10 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the supplementary rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["markov"], default=None,
+                    help="time one supplementary row alone and print it (profiling runs)")
+    ap.add_argument("--markov-positions", type=int, default=None,
+                    help="with --only markov: draft this many positions instead of 16")
     return ap.parse_args()
 
 
@@ -57,14 +62,14 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def source_digest():
-    """Digest of the CUDA sources; a stored ncu traffic figure is used only if it matches."""
+def source_digest(files):
+    """Digest of the CUDA sources a kernel is built from; a stored ncu traffic figure is used only
+    if it was taken on the same sources."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_token_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in sorted(files):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -76,7 +81,7 @@ def stored_traffic(kernel_key):
     with open(path) as f:
         data = json.load(f)
     ent = data.get(kernel_key)
-    if not ent or ent.get("source_digest") != source_digest():
+    if not ent or ent.get("source_digest") != source_digest(ent.get("sources", [])):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -382,7 +387,58 @@ def bench_rows(steps, warmup):
     rows["scheduled_round_512x16_V129280_bf16"] = {
         "ms": tm * 1e3, "GB_s": nb / tm / 1e9, "positions_per_s": int(sel.sum()) / tm,
         "verified_rows": int(rnd["s"]["total_rows"].item()), "status": int(status.item())}
+    del vin, vt
+
+    rows["markov_draft_256x16_V151936_R256"] = bench_markov(steps, warmup, flush, stream)
     return rows
+
+
+def bench_markov(steps, warmup, flush, stream, positions=None):
+    """DSpark Markov-head drafting: 256 requests x 16 positions, V = 151936, R = 256, bf16.  One
+    call drafts every position (16 position kernels + 16 select kernels).  Algorithmic bytes per
+    call: the backbone read and z written once (2 x 1.245 GB) plus Wt read once per position
+    (77.8 MB, usually from L2 after the first); FLOPs: 2 B R V per position."""
+    import torch
+    import speculative_decoding_verification_token_gb300 as sv
+    from speculative_decoding_verification_token_gb300 import synth
+    w = synth.MARKOV
+    if positions is not None:
+        w = dataclasses.replace(w, K=positions)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = synth.markov_inputs(w, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = sv.workspace(sv.dspark_markov_workspace_bytes(w.B, w.K, w.V, w.R), dev)
+    holder = {}
+
+    def call():
+        holder["o"] = sv.dspark_markov_draft(inp["backbone"], inp["U"], inp["Wt"], inp["anchor"],
+                                             inp["scores"], inp["T"], w.seed, status=status,
+                                             workspace=ws)
+    t = time_calls(call, steps, warmup, flush, stream)
+    assert int(status.item()) == 0, sv.status_string(int(status.item()))
+    sv.sv_profile_enable(True)
+    parts = []
+    for _ in range(max(3, steps // 2)):
+        flush()
+        call()
+        parts.append(sv.sv_profile_read())
+    sv.sv_profile_enable(False)
+    pos_ms = sum(p[0] for p in parts) / len(parts)   # position kernel of k = 1
+    sel_ms = sum(p[1] for p in parts) / len(parts)   # its select kernel
+    tm = sum(t) / len(t)
+    elems = w.B * w.K * w.V
+    bytes_call = 2 * elems * 2 + w.K * w.V * w.R * 2
+    flops_call = 2.0 * w.B * w.R * w.V * w.K
+    pos_bytes = bytes_call / w.K
+    return {
+        "workload": f"{w.B} requests x {w.K} positions, V={w.V}, R={w.R}, bf16",
+        "ms": tm * 1e3, "drafted_positions_per_s": w.B * w.K / tm,
+        "GB_s": bytes_call / tm / 1e9, "TFLOP_s": flops_call / tm / 1e12,
+        "sampled_elements_per_s": elems / tm,
+        "position_kernel_ms": pos_ms, "select_kernel_ms": sel_ms,
+        "position_kernel_GB_s": pos_bytes / (pos_ms * 1e-3) / 1e9,
+        "position_kernel_TFLOP_s": flops_call / w.K / (pos_ms * 1e-3) / 1e12,
+        "launches_per_call": 2 * w.K, "status": int(status.item())}
 
 
 # ---- main ----------------------------------------------------------------------------------------
@@ -409,6 +465,12 @@ def main():
     if world > 1:
         torch.distributed.barrier()
         __graft_entry__.build()
+    if args.only == "markov":
+        flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        row = bench_markov(args.steps, args.warmup, lambda: flush_buf.fill_(1),
+                           torch.cuda.current_stream(), args.markov_positions)
+        print(json.dumps({"row": "markov_draft", **row}))
+        return
 
     res = bench_token(args, rank, world, peaks, peak_src)
     w = res["w"]

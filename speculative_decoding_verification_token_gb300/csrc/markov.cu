@@ -31,7 +31,7 @@ constexpr int kMkCols = 64;                  // vocabulary columns per tile (UMM
 constexpr int kMkRank = 256;                 // R (UMMA K)
 constexpr int kMkKB = kMkRank / 64;          // 128-byte k-blocks per row
 constexpr int kMkStages = 2;                 // Wt / backbone ring depth
-constexpr int kMkEpiWarps = 8;
+constexpr int kMkEpiWarps = 16;            // 4 lane quadrants x 4 column quarters
 constexpr int kMkThreads = 32 * (2 + kMkEpiWarps);
 constexpr uint32_t kMkABytes = kMkKB * kMkRows * 128;     // 64 KB
 constexpr uint32_t kMkBBytes = kMkKB * kMkCols * 128;     // 32 KB per stage
@@ -67,6 +67,59 @@ __device__ __forceinline__ float bf16_round_f(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+struct KeyIdx {
+  float key;
+  int32_t idx;
+};
+
+// Exact race keys of the entries flagged in `surv` (bit j: column c0 + j of this thread's quarter)
+// against the running best; their z is read back from the staged tile row `zrow` (two 16-byte
+// chunks of the 128-byte swizzled row r, chunk index cq and cq + 1).  Rare: out of line.
+__device__ __noinline__ KeyIdx markov_survivors(Stream st, uint32_t surv, int64_t c0, int64_t V,
+                                                const uint8_t* tile, uint32_t r, uint32_t cq,
+                                                KeyIdx best) {
+  while (surv) {
+    const uint32_t j = __ffs(surv) - 1;
+    surv &= surv - 1;
+    const int64_t e = c0 + j;
+    if (e >= V) continue;
+    const uint16_t zbits =
+        *reinterpret_cast<const uint16_t*>(tile + tc::sw128(r, cq + (j >> 3)) + 2 * (j & 7));
+    const float z = __uint_as_float(uint32_t(zbits) << 16);
+    if (!(z > -INFINITY)) continue;
+    const uint4 blk = stream_block(st, static_cast<uint32_t>(e >> 2));
+    const float key = z + race_noise(uniform_of(word_of(blk, j & 3)));
+    if (race_better(key, static_cast<int32_t>(e), best.key, best.idx)) {
+      best.key = key;
+      best.idx = static_cast<int32_t>(e);
+    }
+  }
+  return best;
+}
+
+// z = bf16(acc + backbone) for 16 columns: packed bf16 pairs for the store, fp32 values for the
+// statistics and the race.  `valid` < 16 (the tile that crosses V) sets the columns from `valid`
+// on to -inf: they hold zero-filled operands.
+__device__ __forceinline__ void markov_round(float* v, const uint4& bb0, const uint4& bb1,
+                                             int valid, uint32_t* zp) {
+  float bb[16];
+  Elem<bf16_tag>::unpack(bb0, bb);
+  Elem<bf16_tag>::unpack(bb1, bb + 8);
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const __nv_bfloat162 z2 = __floats2bfloat162_rn(v[j] + bb[j], v[j + 1] + bb[j + 1]);
+    zp[j / 2] = *reinterpret_cast<const uint32_t*>(&z2);
+    const float2 zf = __bfloat1622float2(z2);
+    v[j] = zf.x;
+    v[j + 1] = zf.y;
+  }
+  if (valid < 16) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j >= valid) v[j] = -INFINITY;
+  }
+}
+
 template <int kDummy = 0>
 __global__ void __launch_bounds__(kMkThreads, 1)
     markov_position_kernel(const __grid_constant__ CUtensorMap map_wt,
@@ -83,7 +136,7 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   __shared__ uint64_t bb_full[kMkStages], bb_empty[kMkStages];
   __shared__ uint64_t acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base;
-  __shared__ float merge[kMkRows][5];
+  __shared__ float merge[3][kMkRows][5];  // column quarters 1..3 -> quarter 0
   __shared__ uint32_t gate[kGateBuckets];
   __shared__ int32_t s_bad;
 
@@ -178,95 +231,98 @@ __global__ void __launch_bounds__(kMkThreads, 1)
     }
   } else {
     // ---- epilogue: warp w reads TMEM lane quadrant q = w % 4 (rows 32q .. 32q + 31) and column
-    // half h of each 64-column tile; thread (q, lane) owns request m0 + 32q + lane.
+    // quarter h (16 columns) of each 64-column tile; thread (q, lane) owns request m0 + 32q + lane.
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
-    const int r = 32 * q + lane;
-    const int32_t b = m0 + r;
-    const int etid = tid - 64;             // 0..255 among the epilogue threads
-    const bool issuer = etid == 0;         // issues the z stores
+    const uint32_t r = 32 * q + lane;
+    const int32_t b = m0 + static_cast<int32_t>(r);
+    const bool issuer = tid == 64;  // issues the z stores
     const uint64_t req = b < p.B ? (p.request_ids ? p.request_ids[b] : uint64_t(b)) : 0;
-    const Stream st = make_stream(p.seed, req, static_cast<uint32_t>(p.k), 0u /* DRAFT */);
-    float m2 = kM2Empty, s = 0.f, zmax = -INFINITY, best = -INFINITY;
-    int32_t best_idx = -1;
+    const Stream st = make_stream(p.seed, req, static_cast<uint32_t>(p.k), kTagDraft);
+    float m2 = kM2Empty, s = 0.f, zmax = -INFINITY;
+    KeyIdx best = {-INFINITY, -1};
     bool failed = false;
     for (int t = 0; t < n_my; ++t) {
       const int32_t n = ci + t * p.per_mblock;
       const int sb = t % kMkStages;
       const int acc = t & 1;
-      float v[32];
+      float v[16];
       if (!failed && !mbar_wait(&acc_full[acc], (t >> 1) & 1, p.status)) failed = true;
       __syncwarp();
       tc::fence_after_sync();
-      tc::tmem_load32(tmem + (uint32_t(32 * q) << 16) + acc * kMkCols + h * 32, v);
+      tc::tmem_load16(tmem + (uint32_t(32 * q) << 16) + acc * kMkCols + h * 16, v);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
       if (!failed && !mbar_wait(&bb_full[sb], (t / kMkStages) & 1, p.status)) failed = true;
-      uint4 bbv[4];
-      {
-        const uint8_t* tile = sBB + sb * kMkBBBytes;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          bbv[c] = *reinterpret_cast<const uint4*>(tile + tc::sw128(r, 4 * h + c));
-      }
+      const uint8_t* bt = sBB + sb * kMkBBBytes;
+      const uint4 bb0 = *reinterpret_cast<const uint4*>(bt + tc::sw128(r, 2 * h));
+      const uint4 bb1 = *reinterpret_cast<const uint4*>(bt + tc::sw128(r, 2 * h + 1));
       __syncwarp();
       if (lane == 0) mbar_arrive(&bb_empty[sb]);
-      // z = bf16(acc + backbone); columns past V become -inf (they hold zero-filled operands)
-      const int64_t c0 = int64_t(n) * kMkCols + h * 32;
-      uint32_t zp[16];
+      const int64_t c0 = int64_t(n) * kMkCols + h * 16;
+      const int valid = static_cast<int>(p.V - c0 < 16 ? (p.V - c0 > 0 ? p.V - c0 : 0) : 16);
+      uint32_t zp[8];
+      markov_round(v, bb0, bb1, valid, zp);
+      // stage the z tile: source of the TMA store and of the survivors' re-read.  Buffer t & 1 was
+      // last read by the store of tile t - 2, which finished reading before the barrier of tile
+      // t - 1 (the issuer waits for it there).
+      uint8_t* zt = sZ + (t & 1) * kMkZBytes;
+      *reinterpret_cast<uint4*>(zt + tc::sw128(r, 2 * h)) = make_uint4(zp[0], zp[1], zp[2], zp[3]);
+      *reinterpret_cast<uint4*>(zt + tc::sw128(r, 2 * h + 1)) =
+          make_uint4(zp[4], zp[5], zp[6], zp[7]);
+      // softmax statistics (log2 domain): one rescale per tile, then e_j = 2^(z_j log2e - m2)
+      float tmax = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float bb[8];
-        Elem<bf16_tag>::unpack(bbv[c], bb);
+      for (int j = 0; j < 16; ++j) tmax = fmaxf(tmax, v[j]);
+      zmax = fmaxf(zmax, tmax);
+      const float vm = tmax * kLog2e;
+      if (vm > m2) {
+        s *= fast_exp2(m2 - vm);
+        m2 = vm;
+      }
+      float e[16];
 #pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          const __nv_bfloat162 z2 = __floats2bfloat162_rn(v[8 * c + j] + bb[j],
-                                                          v[8 * c + j + 1] + bb[j + 1]);
-          zp[4 * c + j / 2] = *reinterpret_cast<const uint32_t*>(&z2);
-          const float2 zf = __bfloat1622float2(z2);
-          v[8 * c + j] = c0 + 8 * c + j < p.V ? zf.x : -INFINITY;
-          v[8 * c + j + 1] = c0 + 8 * c + j + 1 < p.V ? zf.y : -INFINITY;
+      for (int j = 0; j < 16; ++j) e[j] = fast_exp2(fmaf(v[j], kLog2e, -m2));
+      {
+        float part[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part[j] = e[j] + e[j + 8];
+        s += ((part[0] + part[4]) + (part[2] + part[6])) + ((part[1] + part[5]) + (part[3] + part[7]));
+      }
+      // exponential race, key z_j + G_j with G_j = -log(-log u_j).  Entry j can reach the
+      // running best K only if G_j >= K - z_j; since G <= -log(1 - u) and
+      // 1 - u > ((~w) >> 9) 2^-23, that needs ((~w) >> 9) <= 2^((z_j - K) log2e + 23)
+      // = e_j 2^(m2 + 23 - K log2e).  The 1e-3 margin covers the binary32 rounding of both
+      // sides; the few entries that pass are keyed exactly (markov_survivors).
+      {
+        if (best.idx < 0 && tmax > -INFINITY) {
+          // first finite tile: seed K with the exact key of the tile's largest z
+          uint32_t top = 0;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) top |= (v[j] == tmax ? 1u : 0u) << j;
+          best = markov_survivors(st, top, c0, p.V, zt, r, 2 * h, best);
         }
-      }
-      // softmax statistics (log2 domain) and the largest z
+        const float C = fast_exp2(m2 + 23.0f - best.key * kLog2e) * 1.001f;
+        // rej collects, most significant first, the sign of e_j C - ((~w) >> 9): set = rejected
+        // (fma rounds the exact difference once, so its sign is exact)
+        uint32_t rej = 0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float* x = v + 8 * c;
-        const float vmax = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
-                                 fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
-        zmax = fmaxf(zmax, vmax);
-        ms2_fold(m2, s, x, vmax, 8);
-      }
-      // exponential race: entry e keys z_e - log(-log u_e); the noise gate against the running
-      // best key rejects most entries on the Philox word alone
+        for (int g = 0; g < 4; ++g) {
+          const uint4 blk = stream_block(st, static_cast<uint32_t>((c0 >> 2) + g));
+          const uint32_t w4[4] = {blk.x, blk.y, blk.z, blk.w};
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const uint4 blk = stream_block(st, static_cast<uint32_t>((c0 >> 2) + g));
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float z = v[4 * g + j];
-          const uint32_t w = word_of(blk, j);
-          if (z > -INFINITY && gate_passes(gate, best, z, w)) {
-            const float key = z + race_noise(uniform_of(w));
-            const int32_t e = static_cast<int32_t>(c0 + 4 * g + j);
-            if (race_better(key, e, best, best_idx)) {
-              best = key;
-              best_idx = e;
-            }
+          for (int j = 0; j < 4; ++j) {
+            const float mf = __uint_as_float((w4[j] >> 9) ^ 0x4B7FFFFFu) - 8388608.0f;
+            rej = __funnelshift_l(__float_as_uint(fmaf(e[4 * g + j], C, -mf)), rej, 1);
           }
         }
+        const uint32_t surv = __brev(~rej) >> 16;  // bit j: entry j may beat K
+        if (surv) best = markov_survivors(st, surv, c0, p.V, zt, r, 2 * h, best);
       }
       if (p.write_z) {
-        // sZ[t & 1] is free once the store issued two tiles ago has read it
-        if (issuer) tc::bulk_wait_read<1>();
-        named_sync(1, 32 * kMkEpiWarps);
-        uint8_t* zt = sZ + (t & 1) * kMkZBytes;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(zt + tc::sw128(r, 4 * h + c)) =
-              make_uint4(zp[4 * c], zp[4 * c + 1], zp[4 * c + 2], zp[4 * c + 3]);
         fence_proxy_async();
+        if (issuer) tc::bulk_wait_read<0>();  // the store of tile t - 1 has read its buffer
         named_sync(1, 32 * kMkEpiWarps);
         if (issuer) {
           tc::tma_store_3d(&map_z, zt, n * kMkCols, p.k - 1, m0);
@@ -274,29 +330,32 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         }
       }
     }
-    // fold the two column halves of every request and publish this CTA's partial
-    if (h == 1) {
-      merge[r][0] = m2;
-      merge[r][1] = s;
-      merge[r][2] = zmax;
-      merge[r][3] = best;
-      merge[r][4] = __int_as_float(best_idx);
+    // fold the four column quarters of every request and publish this CTA's partial
+    if (h > 0) {
+      merge[h - 1][r][0] = m2;
+      merge[h - 1][r][1] = s;
+      merge[h - 1][r][2] = zmax;
+      merge[h - 1][r][3] = best.key;
+      merge[h - 1][r][4] = __int_as_float(best.idx);
     }
     named_sync(1, 32 * kMkEpiWarps);
     if (h == 0 && b < p.B) {
-      ms2_merge(m2, s, merge[r][0], merge[r][1]);
-      zmax = fmaxf(zmax, merge[r][2]);
-      const int32_t i2 = __float_as_int(merge[r][4]);
-      if (race_better(merge[r][3], i2, best, best_idx)) {
-        best = merge[r][3];
-        best_idx = i2;
+#pragma unroll
+      for (int hh = 0; hh < 3; ++hh) {
+        ms2_merge(m2, s, merge[hh][r][0], merge[hh][r][1]);
+        zmax = fmaxf(zmax, merge[hh][r][2]);
+        const int32_t i2 = __float_as_int(merge[hh][r][4]);
+        if (race_better(merge[hh][r][3], i2, best.key, best.idx)) {
+          best.key = merge[hh][r][3];
+          best.idx = i2;
+        }
       }
       MkPartial out;
       out.m2 = m2;
       out.s = s;
       out.zmax = zmax;
-      out.key = best;
-      out.idx = best_idx;
+      out.key = best.key;
+      out.idx = best.idx;
       out.pad[0] = out.pad[1] = out.pad[2] = 0;
       p.partials[size_t(b) * p.per_mblock + ci] = out;
     }

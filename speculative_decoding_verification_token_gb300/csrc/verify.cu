@@ -2,7 +2,7 @@
 //
 // A verify call is a short chain of kernels on the caller's stream:
 //   stream  persistent, warp-specialised CTAs (one per SM): a producer warp walks this CTA's
-//           items -- a chunk of one (request, position) row pair -- and feeds a four-deep ring of
+//           items -- a chunk of one (request, position) row pair -- and feeds a three-deep ring of
 //           32 KB shared-memory stages with bulk copies; sixteen consumer warps fold every staged
 //           element into log2-domain softmax statistics (stats pass) or into the residual mass of
 //           block verification (resid pass); the last warp to finish an item merges the warps'

@@ -12,7 +12,7 @@
 //               warps 2-9   the epilogue: TMEM -> registers, + backbone, round to bf16, TMA store
 //                           of z, and per request: log2-domain softmax statistics and the
 //                           exponential race x_k = argmax z - log(-log u) (DRAFT tag, position k)
-//                           with the noise gate, written as one partial per (request, CTA).
+//                           behind a noise gate, written as one partial per (request, CTA).
 //   select    folds the partials of every request into x_k, the row statistics of z_k and the
 //             sequential-temperature-scaled confidence conf_k = 1 / (1 + exp(-s_k / T_k)).
 #include <algorithm>
@@ -137,7 +137,6 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   __shared__ uint64_t acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base;
   __shared__ float merge[3][kMkRows][5];  // column quarters 1..3 -> quarter 0
-  __shared__ uint32_t gate[kGateBuckets];
   __shared__ int32_t s_bad;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -161,7 +160,6 @@ __global__ void __launch_bounds__(kMkThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) tc::tmem_alloc(&tmem_base, kMkTmemCols);
-  build_gate(gate);
 
   // A operand: the 128 rows U[x_{k-1}] in the swizzled K-major layout (rows past B use row 0)
   {

@@ -12,7 +12,8 @@
 //         through distributed shared memory -- a lower bound on the winning key;
 //   main  an entry can reach K0 only if its logit is within kMaxNoise of K0 (no uniform needed to
 //         reject the rest) and, given its uniform, only if its noise reaches K0 - t (the noise gate,
-//         an integer compare on the Philox word); the few entries that pass both are keyed exactly.
+//         tested for a whole 16-byte vector at once on its largest Philox word); the entries of the
+//         few vectors that pass are gated one by one and keyed exactly.
 #pragma once
 
 #include "sv_device.cuh"
@@ -45,36 +46,37 @@ __device__ __forceinline__ bool race_active(const RaceSpec& rs, float t, float d
   return rs.resid ? ((d - t) + rs.gap < 0.f) : (t > -INFINITY);
 }
 
-// Exact key of vocabulary entry e (reads the entry again; used on the rare survivors only).
+// Exact key of vocabulary entry e, or -inf if the entry carries no weight (reads the entry again;
+// used on the rare survivors only).
 template <typename E>
 __device__ __noinline__ float exact_key(const RaceSpec& rs, const uint8_t* trow,
                                         const uint8_t* drow, int64_t e) {
   const float t = Elem<E>::load(trow, e);
   const float d = rs.resid ? Elem<E>::load(drow, e) : 0.f;
+  if (!race_active(rs, t, d)) return -INFINITY;
   const uint4 b = stream_block(rs.st, static_cast<uint32_t>(e >> 2));
   return race_key(rs, t, d, race_noise(uniform_of(word_of(b, static_cast<uint32_t>(e & 3)))));
 }
 
-// Noise gate.  An entry whose logit is delta below K0 reaches K0 only if its noise
-// -log(-log u) >= delta, i.e. u >= exp(-exp(-delta)).  gate[k] is that threshold for
-// delta = k / 4 as a bound on the 23-bit numerator (w >> 9) of u, lowered by 4 to absorb the
-// binary32 rounding of the threshold: an entry with delta >= k / 4 + 0.01 and (w >> 9) < gate[k]
-// cannot win.  (The 0.01 margin covers the binary32 rounding of the key itself.)
-constexpr int kGateBuckets = 68;  // quarter nats up to the kMaxNoise floor
+// Largest element of one 16-byte vector of logits.
+template <typename E>
+__device__ __forceinline__ float vec_max(const uint4& v);
 
-__device__ __forceinline__ void build_gate(uint32_t* gate) {
-  for (int k = threadIdx.x; k < kGateBuckets; k += blockDim.x) {
-    const float thr = expf(-expf(-0.25f * float(k)));
-    const float num = floorf(thr * 8388608.0f) - 4.0f;
-    gate[k] = num < 0.f ? 0u : static_cast<uint32_t>(num);
-  }
+template <>
+__device__ __forceinline__ float vec_max<bf16_tag>(const uint4& v) {
+  __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.x),
+                             *reinterpret_cast<const __nv_bfloat162*>(&v.y));
+  const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.z),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&v.w));
+  a = __hmax2(a, b);
+  const uint32_t ab = *reinterpret_cast<const uint32_t*>(&a);
+  return fmaxf(__uint_as_float(ab << 16), __uint_as_float(ab & 0xFFFF0000u));
 }
 
-__device__ __forceinline__ bool gate_passes(const uint32_t* gate, float K0, float t, uint32_t w) {
-  const float delta = K0 - t;
-  if (!(delta > 0.01f)) return true;
-  const int k = min(static_cast<int>((delta - 0.01f) * 4.0f), kGateBuckets - 1);
-  return (w >> 9) >= gate[k];
+template <>
+__device__ __forceinline__ float vec_max<float>(const uint4& v) {
+  return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+               fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
 }
 
 template <typename E>
@@ -82,117 +84,124 @@ __device__ __forceinline__ uint4 load_vec(const uint8_t* row, int64_t first_elem
   return __ldg(reinterpret_cast<const uint4*>(row + first_elem * esize<E>()));
 }
 
-constexpr int kBatch = 2;  // vectors whose loads each thread issues before using any
+// Noise gate.  key <= t + G with G = -log(-log u) <= -log(1 - u), and 1 - u > m 2^-23 with
+// m = (~w) >> 9 = 0x7FFFFF - (w >> 9).  So an entry reaches the bound K only if
+// m <= 2^23 e^(t - K) = 2^(t log2e + c), c = 23 - K log2e.  A whole vector can hold such an
+// entry only if its smallest m -- that of its largest Philox word -- is within the threshold of its
+// largest logit: one integer max per entry and one ex2 per vector reject almost every vector.  The
+// factor 1.001 covers the binary32 rounding of the threshold and of the keys.
+__device__ __forceinline__ float gate_threshold(float t, float c) {
+  return fast_exp2(fmaf(t, kLog2e, c)) * 1.001f;
+}
 
-// Seed pass over vocabulary range [e0, e0 + len): this thread's active entry of largest logit.
+__device__ __forceinline__ float gate_m(uint32_t w) {
+  return static_cast<float>(0x7FFFFFu - (w >> 9));  // exact: below 2^23
+}
+
+constexpr int kSeedBatch = 4;  // vectors whose loads each thread issues before using any (seed)
+constexpr int kBatch = 2;      // the same for the main pass
+
+// Seed pass over vocabulary range [e0, e0 + len): the exact key of this thread's entry of largest
+// logit (-inf if that entry carries no weight) -- a lower bound on the row's winning key.
 template <typename E>
-__device__ __forceinline__ void seed_range(const RaceSpec& rs, const uint8_t* trow,
-                                           const uint8_t* drow, int64_t e0, int32_t len,
-                                           float& bt, int64_t& be) {
+__device__ __forceinline__ float seed_range(const RaceSpec& rs, const uint8_t* trow,
+                                            const uint8_t* drow, int64_t e0, int32_t len) {
   constexpr int kPer = Elem<E>::kPerVec;
   const int nvec = len / kPer;
+  float bt = -INFINITY;
+  int64_t bv = -1;  // first element of the vector holding bt
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += kThreads * kSeedBatch) {
+    uint4 a[kSeedBatch];
+#pragma unroll
+    for (int u = 0; u < kSeedBatch; ++u) {
+      const int v = v0 + u * kThreads;
+      if (v < nvec) a[u] = load_vec<E>(trow, e0 + int64_t(v) * kPer);
+    }
+#pragma unroll
+    for (int u = 0; u < kSeedBatch; ++u) {
+      const int v = v0 + u * kThreads;
+      if (v >= nvec) break;
+      const float m = vec_max<E>(a[u]);
+      if (m > bt) {
+        bt = m;
+        bv = e0 + int64_t(v) * kPer;
+      }
+    }
+  }
+  int64_t be = -1;
+  if (bv >= 0) {
+    float x[8];
+    Elem<E>::unpack(load_vec<E>(trow, bv), x);
+#pragma unroll
+    for (int q = kPer - 1; q >= 0; --q)
+      if (x[q] == bt) be = bv + q;
+  }
+  for (int i = nvec * kPer + threadIdx.x; i < len; i += kThreads) {
+    const float x = Elem<E>::load(trow, e0 + i);
+    if (x > bt) {
+      bt = x;
+      be = e0 + i;
+    }
+  }
+  return be >= 0 ? exact_key<E>(rs, trow, drow, be) : -INFINITY;
+}
+
+// Offers entry e, with logit t and Philox word w, to the race if it passes the gate.
+template <typename E>
+__device__ __forceinline__ void offer(const RaceSpec& rs, const uint8_t* trow,
+                                      const uint8_t* drow, int64_t e, float t, uint32_t w,
+                                      float c, float& bk, int32_t& bi) {
+  if (!(gate_m(w) <= gate_threshold(t, c))) return;
+  const float k = exact_key<E>(rs, trow, drow, e);
+  if (k > -INFINITY && race_better(k, int32_t(e), bk, bi)) {
+    bk = k;
+    bi = int32_t(e);
+  }
+}
+
+// Main pass over [e0, e0 + len) against the lower bound K0: only the target row is read; the
+// draft row is touched for the few entries keyed exactly.
+template <typename E>
+__device__ __forceinline__ void race_range(const RaceSpec& rs, const uint8_t* trow,
+                                           const uint8_t* drow, int64_t e0, int32_t len,
+                                           float K0, float& bk, int32_t& bi) {
+  constexpr int kPer = Elem<E>::kPerVec;
+  const float floor_t = K0 - kMaxNoise;  // no noise lifts a logit below this to K0
+  const float c = 23.0f - K0 * kLog2e;
+  const int nvec = len / kPer;
   for (int v0 = threadIdx.x; v0 < nvec; v0 += kThreads * kBatch) {
-    uint4 a[kBatch], b[kBatch];
+    uint4 a[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int v = v0 + u * kThreads;
-      if (v < nvec) {
-        a[u] = load_vec<E>(trow, e0 + int64_t(v) * kPer);
-        if (rs.resid) b[u] = load_vec<E>(drow, e0 + int64_t(v) * kPer);
-      }
+      if (v < nvec) a[u] = load_vec<E>(trow, e0 + int64_t(v) * kPer);
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int v = v0 + u * kThreads;
       if (v >= nvec) break;
       const int64_t e = e0 + int64_t(v) * kPer;
-      float x[kPer], y[kPer];
+      const float tmax = vec_max<E>(a[u]);
+      if (!(tmax >= floor_t)) continue;
+      // e is a multiple of kPer (>= 4): the vector's words are whole Philox blocks
+      const uint4 b0 = stream_block(rs.st, static_cast<uint32_t>(e >> 2));
+      const uint4 b1 = kPer == 8 ? stream_block(rs.st, static_cast<uint32_t>(e >> 2) + 1) : b0;
+      const uint32_t wmax = max(max(max(b0.x, b0.y), max(b0.z, b0.w)),
+                                max(max(b1.x, b1.y), max(b1.z, b1.w)));
+      if (gate_m(wmax) > gate_threshold(tmax, c)) continue;
+      float x[8];
       Elem<E>::unpack(a[u], x);
-      if (rs.resid) Elem<E>::unpack(b[u], y);
+      const uint32_t w[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int q = 0; q < kPer; ++q) {
-        const float dq = rs.resid ? y[q] : 0.f;
-        if (x[q] > bt && race_active(rs, x[q], dq)) {
-          bt = x[q];
-          be = e + q;
-        }
-      }
-    }
-  }
-  for (int i = nvec * kPer + threadIdx.x; i < len; i += kThreads) {
-    const float x = Elem<E>::load(trow, e0 + i);
-    const float d = rs.resid ? Elem<E>::load(drow, e0 + i) : 0.f;
-    if (x > bt && race_active(rs, x, d)) {
-      bt = x;
-      be = e0 + i;
-    }
-  }
-}
-
-// Main pass over [e0, e0 + len): exact keys for the entries that pass the floor and the gate.
-template <typename E>
-__device__ __forceinline__ void race_range(const RaceSpec& rs, const uint8_t* trow,
-                                           const uint8_t* drow, int64_t e0, int32_t len,
-                                           float floor_t, float K0, const uint32_t* gate,
-                                           float& bk, int32_t& bi) {
-  constexpr int kPer = Elem<E>::kPerVec;
-  const int nvec = len / kPer;
-  for (int v0 = threadIdx.x; v0 < nvec; v0 += kThreads * kBatch) {
-    uint4 a[kBatch], b[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int v = v0 + u * kThreads;
-      if (v < nvec) {
-        a[u] = load_vec<E>(trow, e0 + int64_t(v) * kPer);
-        if (rs.resid) b[u] = load_vec<E>(drow, e0 + int64_t(v) * kPer);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-    const int v = v0 + u * kThreads;
-    if (v >= nvec) break;
-    const int64_t e = e0 + int64_t(v) * kPer;
-    float x[kPer], y[kPer];
-    Elem<E>::unpack(a[u], x);
-    float xm = x[0];
-#pragma unroll
-    for (int q = 1; q < kPer; ++q) xm = fmaxf(xm, x[q]);
-    if (!(xm >= floor_t)) continue;
-    if (rs.resid) Elem<E>::unpack(b[u], y);
-    // e is a multiple of kPer (>= 4): the vector's words are whole Philox blocks
-    const uint4 b0 = stream_block(rs.st, static_cast<uint32_t>(e >> 2));
-    const uint4 b1 = kPer == 8 ? stream_block(rs.st, static_cast<uint32_t>(e >> 2) + 1) : b0;
-    const uint32_t w[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-    uint32_t mask = 0;
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const float dq = rs.resid ? y[q] : 0.f;
-      if (x[q] >= floor_t && race_active(rs, x[q], dq) && gate_passes(gate, K0, x[q], w[q]))
-        mask |= 1u << q;
-    }
-    while (mask) {
-      const int q = __ffs(mask) - 1;
-      mask &= mask - 1;
-      const float k = exact_key<E>(rs, trow, drow, e + q);
-      if (race_better(k, int32_t(e + q), bk, bi)) {
-        bk = k;
-        bi = int32_t(e + q);
-      }
-    }
+      for (int q = 0; q < kPer; ++q) offer<E>(rs, trow, drow, e + q, x[q], w[q], c, bk, bi);
     }
   }
   for (int i = nvec * kPer + threadIdx.x; i < len; i += kThreads) {
     const int64_t e = e0 + i;
     const float x = Elem<E>::load(trow, e);
-    const float d = rs.resid ? Elem<E>::load(drow, e) : 0.f;
-    if (!(x >= floor_t && race_active(rs, x, d))) continue;
+    if (!(x >= floor_t)) continue;
     const uint4 b = stream_block(rs.st, static_cast<uint32_t>(e >> 2));
-    if (!gate_passes(gate, K0, x, word_of(b, static_cast<uint32_t>(e & 3)))) continue;
-    const float k = exact_key<E>(rs, trow, drow, e);
-    if (race_better(k, int32_t(e), bk, bi)) {
-      bk = k;
-      bi = int32_t(e);
-    }
+    offer<E>(rs, trow, drow, e, x, word_of(b, static_cast<uint32_t>(e & 3)), c, bk, bi);
   }
 }
 
@@ -243,7 +252,7 @@ __device__ void race_row_global(const RaceSpec& rs, const uint8_t* trow, const u
     const float d = rs.resid ? Elem<E>::load(drow, e) : 0.f;
     if (!race_active(rs, x, d)) continue;
     const float k = exact_key<E>(rs, trow, drow, e);
-    if (race_better(k, int32_t(e), bk, bi)) {
+    if (k > -INFINITY && race_better(k, int32_t(e), bk, bi)) {
       bk = k;
       bi = int32_t(e);
     }

@@ -319,6 +319,57 @@ __device__ __forceinline__ void ms2_vec_f32(float& m, float& s, const uint4& v) 
   ms2_fold(m, s, x, vmax, 4);
 }
 
+// Fold N 16-byte vectors into (m, s): one maximum over all of them decides a (rare) rescale, then
+// every element costs one fma, one ex2 and one add (the vector's eight summed as a tree).
+template <int N>
+__device__ __forceinline__ void ms2_fold_vecs_bf16(float& m, float& s, const uint4* v) {
+  auto pair = [](uint32_t w) { return *reinterpret_cast<const __nv_bfloat162*>(&w); };
+  __nv_bfloat162 mx = __hmax2(__hmax2(pair(v[0].x), pair(v[0].y)), __hmax2(pair(v[0].z), pair(v[0].w)));
+#pragma unroll
+  for (int u = 1; u < N; ++u)
+    mx = __hmax2(mx, __hmax2(__hmax2(pair(v[u].x), pair(v[u].y)), __hmax2(pair(v[u].z), pair(v[u].w))));
+  const uint32_t ab = *reinterpret_cast<const uint32_t*>(&mx);
+  const float vm = fmaxf(__uint_as_float(ab << 16), __uint_as_float(ab & 0xFFFF0000u)) * kLog2e;
+  if (vm > m) {
+    s *= fast_exp2(m - vm);
+    m = vm;
+  }
+  float tot = 0.f;
+#pragma unroll
+  for (int u = 0; u < N; ++u) {
+    float x[8], e[8];
+    Elem<bf16_tag>::unpack(v[u], x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) e[j] = fast_exp2(fmaf(x[j], kLog2e, -m));
+    tot += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+  }
+  s += tot;
+}
+
+template <int N>
+__device__ __forceinline__ void ms2_fold_vecs_f32(float& m, float& s, const uint4* v) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < N; ++u)
+    mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(v[u].x), __uint_as_float(v[u].y)),
+                         fmaxf(__uint_as_float(v[u].z), __uint_as_float(v[u].w))));
+  const float vm = mx * kLog2e;
+  if (vm > m) {
+    s *= fast_exp2(m - vm);
+    m = vm;
+  }
+  float tot = 0.f;
+#pragma unroll
+  for (int u = 0; u < N; ++u) {
+    const float e0 = fast_exp2(fmaf(__uint_as_float(v[u].x), kLog2e, -m));
+    const float e1 = fast_exp2(fmaf(__uint_as_float(v[u].y), kLog2e, -m));
+    const float e2 = fast_exp2(fmaf(__uint_as_float(v[u].z), kLog2e, -m));
+    const float e3 = fast_exp2(fmaf(__uint_as_float(v[u].w), kLog2e, -m));
+    tot += (e0 + e1) + (e2 + e3);
+  }
+  s += tot;
+}
+
 __device__ __forceinline__ void ms2_one(float& m, float& s, float x) {
   float xs[8] = {x, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   ms2_fold(m, s, xs, x, 1);

@@ -12,12 +12,15 @@
 //           still in L2 when the race reads them again.
 //   decide  one CTA per request: folds the partials of its rows into the row normalisers and
 //           the ratios p(x)/q(x), draws its uniforms, decides the accepted length (token-level)
-//           or the running ratios / thresholds (block), and writes a race descriptor.
+//           or the running ratios / thresholds (block), and writes a race descriptor.  For
+//           token-level verification this runs at the start of the race kernel (every CTA of a
+//           request's cluster decides, rank 0 writes), so the call is two launches.
 //   race    one thread-block cluster per request (up to 8 CTAs, each staging up to 6 slices of
 //           16 KB): exponential race of the correction (or bonus) row; the CTAs share their seed
 //           keys through distributed shared memory so that every slice prunes against the best
 //           key of the whole row, and rank 0 writes the request's outputs.
-// Block verification runs stream(stats) -> rows -> stream(resid) -> decide -> race.
+// Token-level verification runs stream -> race; block verification runs stream(stats) -> rows
+// -> stream(resid) -> decide -> race.
 #include <algorithm>
 #include <mutex>
 
@@ -30,7 +33,9 @@ namespace sv {
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kStreamThreads = kConsumers + 32;  // + one producer warp
-constexpr uint32_t kRowBytes = 32768;            // bytes of one row in one stream stage (item)
+constexpr uint32_t kRowBytes = 32768;            // bytes of one row in one stream stage
+constexpr int kStagesPerItem = 2;                // stages of one item (one merge per item)
+constexpr uint32_t kItemBytes = kStagesPerItem * kRowBytes;
 constexpr int kRing = 3;                         // stages of 2 x kRowBytes (target + draft)
 constexpr int kRedBufs = 4;                      // items a consumer warp may run ahead, plus one
 constexpr size_t kStreamSmem = size_t(kRing) * 2 * kRowBytes;
@@ -66,9 +71,9 @@ static inline int32_t slices_of(int64_t V, int esz) {
   return static_cast<int32_t>((V + per - 1) / per);
 }
 
-// Stream items (chunks) per row: one stage of kRowBytes each.
+// Stream items (chunks) per row: up to kStagesPerItem stages of kRowBytes each.
 static inline int32_t chunks_of(int64_t V, int esz) {
-  const int64_t per = kRowBytes / esz;
+  const int64_t per = kItemBytes / esz;
   return static_cast<int32_t>((V + per - 1) / per);
 }
 
@@ -155,16 +160,19 @@ __device__ void stream_producer(const StreamParams& p, uint8_t* ring, uint64_t* 
       gap = (nm.x - nm.z) * kLn2 + (logf(nm.y / nm.w) - logf(rho_prev));
       mt = nm.x;
     }
-    {
+    const int64_t ie0 = int64_t(c) * kSE * kStagesPerItem;
+    const int64_t iend = p.V - ie0 < int64_t(kSE) * kStagesPerItem ? p.V
+                                                                    : ie0 + int64_t(kSE) * kStagesPerItem;
+    for (int64_t e0 = ie0; e0 < iend; e0 += kSE) {
       const uint32_t stage = n % kRing;
       if (n >= kRing && !mbar_wait(&empty[stage], ((n / kRing) - 1) & 1, p.status)) return;
       StageMeta m;
       m.unit = unit;
       m.chunk = c;
-      m.last = 1;
+      m.last = e0 + kSE >= iend;
       m.item = issued;
-      m.e0 = int64_t(c) * kSE;
-      m.len = static_cast<int32_t>(p.V - m.e0 < kSE ? p.V - m.e0 : kSE);
+      m.e0 = e0;
+      m.len = static_cast<int32_t>(iend - e0 < kSE ? iend - e0 : kSE);
       const uint32_t bulk_bytes = (uint32_t(m.len) * esize<E>()) & ~15u;
       m.bulk = static_cast<int32_t>(bulk_bytes / esize<E>());
       m.trow = trow;
@@ -211,7 +219,23 @@ __device__ void stream_consumer(const StreamParams& p, const uint8_t* ring, uint
     const uint4* vt = reinterpret_cast<const uint4*>(ring + size_t(stage) * 2 * kRowBytes);
     const uint4* vd = vt + kRowBytes / 16;
     const int nvec = m.bulk / kPer;
-    if (!p.resid_pass) {
+    if (!p.resid_pass && m.bulk == int32_t(kRowBytes / esize<E>())) {
+      // full stage: every consumer thread holds kFull vectors of each row
+      constexpr int kFull = int(kRowBytes / 16) / kConsumers;
+      static_assert(kFull * kConsumers * 16 == int(kRowBytes), "stage not a whole multiple");
+      uint4 a[kFull], b[kFull];
+#pragma unroll
+      for (int u = 0; u < kFull; ++u) a[u] = vt[tid + u * kConsumers];
+#pragma unroll
+      for (int u = 0; u < kFull; ++u) b[u] = vd[tid + u * kConsumers];
+      if constexpr (kPer == 8) {
+        ms2_fold_vecs_bf16<kFull>(mt, st, a);
+        ms2_fold_vecs_bf16<kFull>(md, sd, b);
+      } else {
+        ms2_fold_vecs_f32<kFull>(mt, st, a);
+        ms2_fold_vecs_f32<kFull>(md, sd, b);
+      }
+    } else if (!p.resid_pass) {
 #pragma unroll 2
       for (int v = tid; v < nvec; v += kConsumers) {
         const uint4 a = vt[v], b = vd[v];
@@ -341,15 +365,19 @@ struct DecideParams {
   int32_t* status;
 };
 
+// The decision of request r by one CTA.  `writer`: this CTA writes the call's outputs (ratios,
+// row normalisers, the race descriptor in the workspace, the status word); `s_desc` (nullable)
+// receives the race descriptor in shared memory.  Every thread of the CTA must call it.
 template <typename E>
-__global__ void __launch_bounds__(kThreads) decide_kernel(DecideParams p) {
+__device__ __noinline__ void decide_body(const DecideParams& p, int32_t r, bool writer,
+                                            RaceDesc* s_desc) {
   __shared__ float s_ratio[SV_MAX_DRAFT_LEN + 1];
   __shared__ float s_rho[SV_MAX_DRAFT_LEN + 1];
   __shared__ float s_R[SV_MAX_DRAFT_LEN + 1];
   __shared__ float s_u[SV_MAX_DRAFT_LEN + 1];
+  __shared__ float4 s_norm[SV_MAX_DRAFT_LEN + 1];
   __shared__ int32_t s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int32_t r = blockIdx.x;
   const int32_t graw = p.draft_len[r];
   const int32_t g = clamp_gamma(graw, p.gmax);
   const uint64_t req = p.request_ids ? p.request_ids[r] : uint64_t(r);
@@ -386,7 +414,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(DecideParams p) {
         }
         if (bad) s_bad = SV_ERR_BAD_INPUT;
         s_ratio[i] = ratio;
-        __stcg(&p.ws.norms[unit], make_float4(mt, st, md, sd));
+        s_norm[i] = make_float4(mt, st, md, sd);
+        if (writer) __stcg(&p.ws.norms[unit], s_norm[i]);
       }
     }
   } else {
@@ -408,7 +437,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(DecideParams p) {
   __syncthreads();
 
   if (tid == 0) {
-    if (s_bad) report(p.status, s_bad);
+    if (writer && s_bad) report(p.status, s_bad);
     RowInfo* rows = p.ws.rows + size_t(r) * p.gmax;
     if (p.mode == 1) {
       // running capped ratios rho_i = min(1, rho_{i-1} p_i(x_i) / q_i(x_i))
@@ -449,15 +478,22 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(DecideParams p) {
       d.gap = 0.f;
       d.pad = 0;
       if (d.resid) {
-        const float4 nm = __ldcg(&p.ws.norms[r * p.gmax + tau]);
+        // token-level: this CTA's own normalisers; block: those of the rows kernel
+        const float4 nm = p.mode == 0 ? s_norm[tau + 1] : __ldcg(&p.ws.norms[r * p.gmax + tau]);
         d.gap = (nm.x - nm.z) * kLn2 + logf(nm.y / nm.w) - lnw;
       }
-      p.ws.desc[r] = d;
+      if (writer) p.ws.desc[r] = d;
+      if (s_desc) *s_desc = d;
     }
   }
-  if (p.mode == 0 && p.ratio_out)
+  if (writer && p.mode == 0 && p.ratio_out)
     for (int i = tid + 1; i <= g; i += kThreads)
       p.ratio_out[p.draft_row0[r] + (i - 1)] = fminf(1.f, s_ratio[i]);
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kThreads) decide_kernel(DecideParams p) {
+  decide_body<E>(p, blockIdx.x, true, nullptr);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -483,6 +519,8 @@ struct RaceParams {
   int32_t* sampled_tokens;  // sampler output, indexed like the draft rows
   VerifyWs ws;
   int32_t* status;
+  int32_t fused;            // token-level verify: decide in this kernel (dp), rank 0 writing
+  DecideParams dp;
 };
 
 template <typename E>
@@ -493,7 +531,6 @@ __global__ void __launch_bounds__(kThreads, 4) race_kernel(RaceParams p) {
   __shared__ float s_best_k;
   __shared__ int32_t s_best_i;
   __shared__ float s_K0;
-  __shared__ uint32_t gate[kGateBuckets];
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t rank = cluster_rank();
   const int32_t job = blockIdx.x / p.CL;
@@ -507,7 +544,12 @@ __global__ void __launch_bounds__(kThreads, 4) race_kernel(RaceParams p) {
   int64_t sample_row = 0;
   if (!p.sampler) {
     r = job;
-    const RaceDesc d = p.ws.desc[r];
+    __shared__ RaceDesc s_desc;
+    if (p.fused) {
+      decide_body<E>(p.dp, r, rank == 0, &s_desc);
+      __syncthreads();
+    }
+    const RaceDesc d = p.fused ? s_desc : p.ws.desc[r];
     tau = d.tau;
     rs.resid = d.resid != 0;
     rs.gap = d.gap;
@@ -531,7 +573,6 @@ __global__ void __launch_bounds__(kThreads, 4) race_kernel(RaceParams p) {
   }
   const uint64_t req = p.request_ids ? p.request_ids[r] : uint64_t(r);
   rs.st = make_stream(p.seed, req, pos, p.sampler ? kTagDraft : (rs.resid ? kTagResid : kTagBonus));
-  build_gate(gate);
 
   // this CTA's share of the row: a contiguous range, a whole number of 16-byte vectors long
   constexpr int32_t kPer = Elem<E>::kPerVec;
@@ -540,10 +581,7 @@ __global__ void __launch_bounds__(kThreads, 4) race_kernel(RaceParams p) {
   const int64_t hi = min(p.V, lo + share);
 
   // seed: every thread's largest-logit entry of the share
-  float bt = -INFINITY;
-  int64_t be = -1;
-  if (active) seed_range<E>(rs, trow, drow, lo, int32_t(hi - lo), bt, be);
-  float seed = be >= 0 ? exact_key<E>(rs, trow, drow, be) : -INFINITY;
+  float seed = active ? seed_range<E>(rs, trow, drow, lo, int32_t(hi - lo)) : -INFINITY;
   seed = block_max(seed, red_k);
   if (tid == 0) s_seed = seed;
   cluster_sync();
@@ -558,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 4) race_kernel(RaceParams p) {
   // main pass: only entries within kMaxNoise of K0 whose noise can reach K0 are keyed
   float bk = -INFINITY;
   int32_t bi = -1;
-  if (active) race_range<E>(rs, trow, drow, lo, int32_t(hi - lo), K0 - kMaxNoise, K0, gate, bk, bi);
+  if (active) race_range<E>(rs, trow, drow, lo, int32_t(hi - lo), K0, bk, bi);
   block_race(bk, bi, red_k, red_i);
   if (tid == 0) {
     s_best_k = bk;
@@ -730,9 +768,8 @@ static sv_status run_verify(bool block, const CommonArgs& a, const int64_t* targ
   dp.ws = ws;
   dp.status = status;
   if (!block) {
-    profile_mark(1, stream);
+    profile_mark(1, stream);  // token-level: the race kernel decides (no kernel in between)
     dp.mode = 0;
-    decide_kernel<E><<<a.B, kThreads, 0, stream>>>(dp);
   } else {
     dp.mode = 1;
     decide_kernel<E><<<a.B, kThreads, 0, stream>>>(dp);
@@ -766,6 +803,8 @@ static sv_status run_verify(bool block, const CommonArgs& a, const int64_t* targ
   rp.correction_token = correction_token;
   rp.ws = ws;
   rp.status = status;
+  rp.fused = block ? 0 : 1;
+  rp.dp = dp;
   st = launch_race<E>(rp, a.B, stream);
   if (st != SV_OK) return st;
   profile_mark(3, stream);

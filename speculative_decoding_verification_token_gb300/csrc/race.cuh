@@ -1,15 +1,16 @@
-// race.cuh -- the exponential race over a row (or a row pair for residuals) split across the CTAs
-// of a thread-block cluster.
+// race.cuh -- the exponential race over a row (or a row pair for residuals) split across CTAs.
 //
 // The key of entry x is log w(x) - log E_x (E_x = -log u_x); the largest key wins, equal keys go to
 // the lower index.  Residual entries (weight max(w p(x) - q(x), 0)) are written, up to a per-row
 // constant, t + log(1 - exp(y)) - log E with y = (d - t) + gap; plain entries (a row sampled
 // from its own softmax) t - log E.  Either way key <= t + noise with noise = -log(-log u).
 //
-// Each CTA of the cluster owns one contiguous 1/CL of the row and reads it twice from global
-// memory (the rows were just streamed, so mostly from L2):
-//   seed  every thread keys its entry of largest logit; the cluster shares the best such key K0
-//         through distributed shared memory -- a lower bound on the winning key;
+// Each CTA owns one contiguous 1/CL of the row; its 16-byte vectors come from `vsrc` -- the share
+// staged in shared memory by one bulk copy, or the row itself in global memory -- and are read
+// twice:
+//   seed  every thread keys its entry of largest logit; the best such key of the CTA, raised to
+//         the best that the job's other shares have published, is a lower bound K0 on the winning
+//         key;
 //   main  an entry can reach K0 only if its logit is within kMaxNoise of K0 (no uniform needed to
 //         reject the rest) and, given its uniform, only if its noise reaches K0 - t (the noise gate,
 //         tested for a whole 16-byte vector at once on its largest Philox word); the entries of the
@@ -46,16 +47,45 @@ __device__ __forceinline__ bool race_active(const RaceSpec& rs, float t, float d
   return rs.resid ? ((d - t) + rs.gap < 0.f) : (t > -INFINITY);
 }
 
-// Exact key of vocabulary entry e, or -inf if the entry carries no weight (reads the entry again;
-// used on the rare survivors only).
+// Exact key of vocabulary entry e with logit t, or -inf if the entry carries no weight (reads the
+// draft logit of a residual entry; used on the rare survivors only).
 template <typename E>
-__device__ __noinline__ float exact_key(const RaceSpec& rs, const uint8_t* trow,
-                                        const uint8_t* drow, int64_t e) {
-  const float t = Elem<E>::load(trow, e);
+__device__ __noinline__ float exact_key_t(const RaceSpec& rs, float t, const uint8_t* drow,
+                                          int64_t e) {
   const float d = rs.resid ? Elem<E>::load(drow, e) : 0.f;
   if (!race_active(rs, t, d)) return -INFINITY;
   const uint4 b = stream_block(rs.st, static_cast<uint32_t>(e >> 2));
   return race_key(rs, t, d, race_noise(uniform_of(word_of(b, static_cast<uint32_t>(e & 3)))));
+}
+
+template <typename E>
+__device__ __forceinline__ float exact_key(const RaceSpec& rs, const uint8_t* trow,
+                                           const uint8_t* drow, int64_t e) {
+  return exact_key_t<E>(rs, Elem<E>::load(trow, e), drow, e);
+}
+
+// A race result as one 64-bit word whose unsigned order is the race order: the key's bits made
+// order-preserving in the high half, the complemented index in the low half (equal keys: the
+// lower index is larger).  0 is below every packed result.
+__device__ __forceinline__ unsigned long long race_pack(float key, int32_t idx) {
+  const uint32_t u = __float_as_uint(key);
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(o) << 32) | static_cast<uint32_t>(~idx);
+}
+
+__device__ __forceinline__ int32_t race_unpack_index(unsigned long long packed) {
+  return static_cast<int32_t>(~static_cast<uint32_t>(packed));
+}
+
+// Order-preserving bits of a key (the high half of race_pack) and back; 0 decodes to -inf.
+__device__ __forceinline__ uint32_t key_order(float key) {
+  const uint32_t u = __float_as_uint(key);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_from_order(uint32_t o) {
+  if (o == 0) return -INFINITY;
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
 // Largest element of one 16-byte vector of logits.
@@ -79,11 +109,6 @@ __device__ __forceinline__ float vec_max<float>(const uint4& v) {
                fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
 }
 
-template <typename E>
-__device__ __forceinline__ uint4 load_vec(const uint8_t* row, int64_t first_elem) {
-  return __ldg(reinterpret_cast<const uint4*>(row + first_elem * esize<E>()));
-}
-
 // Noise gate.  key <= t + G with G = -log(-log u) <= -log(1 - u), and 1 - u > m 2^-23 with
 // m = (~w) >> 9 = 0x7FFFFF - (w >> 9).  So an entry reaches the bound K only if
 // m <= 2^23 e^(t - K) = 2^(t log2e + c), c = 23 - K log2e.  A whole vector can hold such an
@@ -102,10 +127,11 @@ constexpr int kSeedBatch = 4;  // vectors whose loads each thread issues before 
 constexpr int kBatch = 2;      // the same for the main pass
 
 // Seed pass over vocabulary range [e0, e0 + len): the exact key of this thread's entry of largest
-// logit (-inf if that entry carries no weight) -- a lower bound on the row's winning key.
+// logit (-inf if that entry carries no weight) -- a lower bound on the range's winning key.
 template <typename E>
-__device__ __forceinline__ float seed_range(const RaceSpec& rs, const uint8_t* trow,
-                                            const uint8_t* drow, int64_t e0, int32_t len) {
+__device__ __forceinline__ float seed_range(const RaceSpec& rs, const uint4* vsrc,
+                                            const uint8_t* trow, const uint8_t* drow, int64_t e0,
+                                            int32_t len) {
   constexpr int kPer = Elem<E>::kPerVec;
   const int nvec = len / kPer;
   float bt = -INFINITY;
@@ -115,7 +141,7 @@ __device__ __forceinline__ float seed_range(const RaceSpec& rs, const uint8_t* t
 #pragma unroll
     for (int u = 0; u < kSeedBatch; ++u) {
       const int v = v0 + u * kThreads;
-      if (v < nvec) a[u] = load_vec<E>(trow, e0 + int64_t(v) * kPer);
+      if (v < nvec) a[u] = vsrc[v];
     }
 #pragma unroll
     for (int u = 0; u < kSeedBatch; ++u) {
@@ -131,7 +157,7 @@ __device__ __forceinline__ float seed_range(const RaceSpec& rs, const uint8_t* t
   int64_t be = -1;
   if (bv >= 0) {
     float x[8];
-    Elem<E>::unpack(load_vec<E>(trow, bv), x);
+    Elem<E>::unpack(vsrc[(bv - e0) / kPer], x);
 #pragma unroll
     for (int q = kPer - 1; q >= 0; --q)
       if (x[q] == bt) be = bv + q;
@@ -143,7 +169,7 @@ __device__ __forceinline__ float seed_range(const RaceSpec& rs, const uint8_t* t
       be = e0 + i;
     }
   }
-  return be >= 0 ? exact_key<E>(rs, trow, drow, be) : -INFINITY;
+  return be >= 0 ? exact_key_t<E>(rs, bt, drow, be) : -INFINITY;
 }
 
 // Offers entry e, with logit t and Philox word w, to the race if it passes the gate.
@@ -152,7 +178,7 @@ __device__ __forceinline__ void offer(const RaceSpec& rs, const uint8_t* trow,
                                       const uint8_t* drow, int64_t e, float t, uint32_t w,
                                       float c, float& bk, int32_t& bi) {
   if (!(gate_m(w) <= gate_threshold(t, c))) return;
-  const float k = exact_key<E>(rs, trow, drow, e);
+  const float k = exact_key_t<E>(rs, t, drow, e);
   if (k > -INFINITY && race_better(k, int32_t(e), bk, bi)) {
     bk = k;
     bi = int32_t(e);
@@ -162,9 +188,9 @@ __device__ __forceinline__ void offer(const RaceSpec& rs, const uint8_t* trow,
 // Main pass over [e0, e0 + len) against the lower bound K0: only the target row is read; the
 // draft row is touched for the few entries keyed exactly.
 template <typename E>
-__device__ __forceinline__ void race_range(const RaceSpec& rs, const uint8_t* trow,
-                                           const uint8_t* drow, int64_t e0, int32_t len,
-                                           float K0, float& bk, int32_t& bi) {
+__device__ __forceinline__ void race_range(const RaceSpec& rs, const uint4* vsrc,
+                                           const uint8_t* trow, const uint8_t* drow, int64_t e0,
+                                           int32_t len, float K0, float& bk, int32_t& bi) {
   constexpr int kPer = Elem<E>::kPerVec;
   const float floor_t = K0 - kMaxNoise;  // no noise lifts a logit below this to K0
   const float c = 23.0f - K0 * kLog2e;
@@ -174,7 +200,7 @@ __device__ __forceinline__ void race_range(const RaceSpec& rs, const uint8_t* tr
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int v = v0 + u * kThreads;
-      if (v < nvec) a[u] = load_vec<E>(trow, e0 + int64_t(v) * kPer);
+      if (v < nvec) a[u] = vsrc[v];
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
@@ -260,29 +286,6 @@ __device__ void race_row_global(const RaceSpec& rs, const uint8_t* trow, const u
   block_race(bk, bi, red_k, red_i);
   out_key = bk;
   out_idx = bi;
-}
-
-// ---- thread-block clusters --------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::
-          : "memory");
-}
-
-// Read a 32-bit word at the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t dsmem_load_u32(const void* local, uint32_t rank) {
-  uint32_t remote, v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)),
-               "r"(rank));
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
-  return v;
 }
 
 }  // namespace sv

@@ -14,11 +14,13 @@
 //           the ratios p(x)/q(x), draws its uniforms, decides the accepted length (token-level)
 //           or the running ratios / thresholds (block), and writes a race descriptor.  For
 //           token-level verification this runs at the start of the race kernel (every CTA of a
-//           request's cluster decides, rank 0 writes), so the call is two launches.
-//   race    one thread-block cluster per request (up to 8 CTAs, each staging up to 6 slices of
-//           16 KB): exponential race of the correction (or bonus) row; the CTAs share their seed
-//           keys through distributed shared memory so that every slice prunes against the best
-//           key of the whole row, and rank 0 writes the request's outputs.
+//           request decides, the first writes), so the call is two launches.
+//   race    up to 8 CTAs per request, each staging its contiguous share of the correction (or
+//           bonus) row in shared memory with one bulk copy: exponential race of the share, pruned
+//           against the best seed key any share has published; the shares combine through one
+//           64-bit atomic max per request and the last share to finish writes the outputs.  It is
+//           launched as a programmatic dependent of the stream kernel, so its launch overlaps the
+//           stream's tail.
 // Token-level verification runs stream -> race; block verification runs stream(stats) -> rows
 // -> stream(resid) -> decide -> race.
 #include <algorithm>
@@ -39,7 +41,8 @@ constexpr uint32_t kItemBytes = kStagesPerItem * kRowBytes;
 constexpr int kRing = 3;                         // stages of 2 x kRowBytes (target + draft)
 constexpr int kRedBufs = 4;                      // items a consumer warp may run ahead, plus one
 constexpr size_t kStreamSmem = size_t(kRing) * 2 * kRowBytes;
-constexpr int kRaceClusterMax = 8;               // CTAs per race cluster (portable size)
+constexpr int kRaceSplitMax = 8;                 // CTAs (row shares) per race job
+constexpr uint32_t kRaceShareMax = 64 * 1024;    // largest row share staged in shared memory
 
 struct RowInfo {  // one (request, position) row pair
   float ratio;    // p(x)/q(x) of the drafted token x
@@ -55,12 +58,19 @@ struct RaceDesc {  // per request, written by decide, read by race
   int32_t pad;
 };
 
+struct RaceSlot {                 // per race job: the shares' combined winner
+  unsigned long long best;        // race_pack(key, index); 0: no candidate yet
+  uint32_t count;                 // shares finished
+  uint32_t k0;                    // key_order of the best seed key published so far (0: none)
+};
+
 struct VerifyWs {
   float4* partials;  // [units * C] (m_t, s_t, m_d, s_d), m in log2 units
   float4* norms;     // [units] statistics of the whole row pair
   RowInfo* rows;     // [units]
   float* rpart;      // [units * C] residual mass per chunk (block)
   RaceDesc* desc;    // [B]
+  RaceSlot* slots;   // [units]: verify uses B of them, the sampler one per drafted row
   size_t total;
 };
 
@@ -93,6 +103,7 @@ static VerifyWs verify_layout(void* base, int32_t B, int32_t gmax, int32_t C) {
   w.rows = reinterpret_cast<RowInfo*>(take(sizeof(RowInfo) * units));
   w.rpart = reinterpret_cast<float*>(take(sizeof(float) * units * size_t(C)));
   w.desc = reinterpret_cast<RaceDesc*>(take(sizeof(RaceDesc) * Bn));
+  w.slots = reinterpret_cast<RaceSlot*>(take(sizeof(RaceSlot) * units));
   w.total = off;
   return w;
 }
@@ -336,6 +347,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(StreamParams 
     for (int k = 0; k < kRedBufs; ++k) ms.count[k] = 0;
     fence_barrier_init();
   }
+  // the race kernel that follows may launch now (it waits for this grid's results itself)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == 0)  // the race's per-request slots start empty
+    for (int i = threadIdx.x; i < p.B; i += blockDim.x) p.ws.slots[i] = RaceSlot{0ull, 0u, 0u};
   __syncthreads();
   if (warp == kConsumerWarps) {
     if ((threadIdx.x & 31) == 0) stream_producer<E>(p, ring, full, empty, meta);
@@ -497,8 +512,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(DecideParams p) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// race: one cluster per job -- the correction / bonus token of a request (verify), or one
-// drafted token (sampler)
+// race: CL CTAs per job -- the correction / bonus token of a request (verify), or one drafted
+// token (sampler)
 // ---------------------------------------------------------------------------------------------
 struct RaceParams {
   const uint8_t* target;  // verify: target logits; sampler: the draft logits
@@ -508,7 +523,7 @@ struct RaceParams {
   const int64_t* draft_row0;
   const int32_t* draft_len;
   const int32_t* draft_tokens;
-  int32_t B, gmax, S, CL;  // 16 KB slices per row, CTAs per cluster
+  int32_t B, gmax, S, CL;  // 16 KB slices per row, CTAs (row shares) per job
   int32_t sampler;
   uint64_t seed;
   const uint64_t* request_ids;
@@ -520,20 +535,25 @@ struct RaceParams {
   VerifyWs ws;
   int32_t* status;
   int32_t fused;            // token-level verify: decide in this kernel (dp), rank 0 writing
+  int32_t stage_share;      // the launch provides dynamic shared memory for the row share
   DecideParams dp;
 };
 
 template <typename E>
 __global__ void __launch_bounds__(kThreads, 4) race_kernel(RaceParams p) {
+  extern __shared__ __align__(128) uint8_t share_sm[];  // this CTA's share of the row (staged)
+  __shared__ uint64_t share_bar;
   __shared__ float red_k[kWarps];
   __shared__ int32_t red_i[kWarps];
-  __shared__ float s_seed;
-  __shared__ float s_best_k;
-  __shared__ int32_t s_best_i;
-  __shared__ float s_K0;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const uint32_t rank = cluster_rank();
+  __shared__ int32_t s_last;
+  __shared__ int32_t s_winner;
+  __shared__ float s_k0;
+  __shared__ RaceDesc s_desc;
+  const int tid = threadIdx.x;
   const int32_t job = blockIdx.x / p.CL;
+  const int32_t part = blockIdx.x - job * p.CL;  // this CTA's share of the job's row
+  // launched as a programmatic dependent of the previous kernel: wait for its results
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // resolve the job
   bool active = true;
@@ -544,9 +564,8 @@ __global__ void __launch_bounds__(kThreads, 4) race_kernel(RaceParams p) {
   int64_t sample_row = 0;
   if (!p.sampler) {
     r = job;
-    __shared__ RaceDesc s_desc;
     if (p.fused) {
-      decide_body<E>(p.dp, r, rank == 0, &s_desc);
+      decide_body<E>(p.dp, r, part == 0, &s_desc);
       __syncthreads();
     }
     const RaceDesc d = p.fused ? s_desc : p.ws.desc[r];
@@ -561,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 4) race_kernel(RaceParams p) {
     pos = job - r * p.gmax + 1;
     const int32_t g = p.draft_len[r];
     if (g < 0 || g > p.gmax) {
-      if (tid == 0 && rank == 0 && pos == 1) report(p.status, SV_ERR_BAD_INPUT);
+      if (tid == 0 && part == 0 && pos == 1) report(p.status, SV_ERR_BAD_INPUT);
       active = false;
     } else if (pos > g) {
       active = false;
@@ -577,73 +596,84 @@ __global__ void __launch_bounds__(kThreads, 4) race_kernel(RaceParams p) {
   // this CTA's share of the row: a contiguous range, a whole number of 16-byte vectors long
   constexpr int32_t kPer = Elem<E>::kPerVec;
   const int64_t share = (p.V + int64_t(p.CL) * kPer - 1) / (int64_t(p.CL) * kPer) * kPer;
-  const int64_t lo = min(p.V, int64_t(rank) * share);
+  const int64_t lo = min(p.V, int64_t(part) * share);
   const int64_t hi = min(p.V, lo + share);
 
-  // seed: every thread's largest-logit entry of the share
-  float seed = active ? seed_range<E>(rs, trow, drow, lo, int32_t(hi - lo)) : -INFINITY;
-  seed = block_max(seed, red_k);
-  if (tid == 0) s_seed = seed;
-  cluster_sync();
-  if (tid < 32) {  // the best seed of the cluster, one DSMEM read per lane
-    float k = lane < p.CL ? __uint_as_float(dsmem_load_u32(&s_seed, lane)) : -INFINITY;
-    k = warp_max(k);
-    if (lane == 0) s_K0 = k;
+  // stage the share's whole 16-byte vectors in shared memory with one bulk copy (shares too
+  // large for it are read from global memory); a ragged tail is read from global memory
+  const uint32_t vec_bytes = static_cast<uint32_t>(((hi - lo) * esize<E>()) & ~int64_t(15));
+  const bool staged = p.stage_share && active && vec_bytes > 0;
+  if (tid == 0 && staged) {
+    mbar_init(&share_bar, 1);
+    fence_barrier_init();
+    mbar_expect_tx(&share_bar, vec_bytes);
+    bulk_g2s(share_sm, trow + lo * esize<E>(), vec_bytes, &share_bar);
   }
   __syncthreads();
-  const float K0 = s_K0;
+  if (staged) mbar_wait(&share_bar, 0, p.status);
+  const uint4* vsrc = staged ? reinterpret_cast<const uint4*>(share_sm)
+                             : reinterpret_cast<const uint4*>(trow + lo * esize<E>());
 
-  // main pass: only entries within kMaxNoise of K0 whose noise can reach K0 are keyed
+  // seed: the best exact key among the threads' largest-logit entries, raised to the best seed
+  // the job's other shares have published so far -- a lower bound on the winning key, against
+  // which the main pass gates
+  RaceSlot* slot = p.ws.slots + job;
+  float seed = active ? seed_range<E>(rs, vsrc, trow, drow, lo, int32_t(hi - lo)) : -INFINITY;
+  seed = block_max(seed, red_k);
+  if (tid == 0) {
+    const uint32_t prev = active ? atomicMax(&slot->k0, key_order(seed)) : 0u;
+    s_k0 = fmaxf(seed, key_from_order(prev));
+  }
+  __syncthreads();
+  const float K0 = s_k0;
+
+  // main pass: only entries whose logit and noise can reach K0 are keyed
   float bk = -INFINITY;
   int32_t bi = -1;
-  if (active) race_range<E>(rs, trow, drow, lo, int32_t(hi - lo), K0, bk, bi);
+  if (active) race_range<E>(rs, vsrc, trow, drow, lo, int32_t(hi - lo), K0, bk, bi);
   block_race(bk, bi, red_k, red_i);
+
+  // combine the shares: a 64-bit max over (order-preserving key bits, ~index), so equal keys go
+  // to the lower index; the last share to arrive writes the job's outputs
   if (tid == 0) {
-    s_best_k = bk;
-    s_best_i = bi;
+    if (bi >= 0) atomicMax(&slot->best, race_pack(bk, bi));
+    __threadfence();
+    s_last = atomicAdd(&slot->count, 1u) == uint32_t(p.CL - 1);
   }
-  cluster_sync();
-  if (rank == 0 && active) {
-    if (tid < 32) {  // winner over the cluster, one DSMEM read pair per lane
-      float k = -INFINITY;
-      int32_t y = -1;
-      if (lane < p.CL) {
-        k = __uint_as_float(dsmem_load_u32(&s_best_k, lane));
-        y = int32_t(dsmem_load_u32(&s_best_i, lane));
-      }
-      warp_race(k, y);
-      if (lane == 0) red_i[0] = y;
+  __syncthreads();
+  if (!s_last || !active) return;
+  if (tid == 0) {
+    __threadfence();
+    const unsigned long long best = atomicAdd(&slot->best, 0ull);
+    s_winner = best ? race_unpack_index(best) : -1;
+  }
+  __syncthreads();
+  int32_t y = s_winner;
+  if (y < 0 && rs.resid) {
+    // residual empty to working precision (p and q agree): draw from p with the same uniforms
+    RaceSpec fb = rs;
+    fb.resid = false;
+    float k;
+    race_row_global<E>(fb, trow, nullptr, p.V, red_k, red_i, k, y);
+  }
+  if (!p.sampler) {
+    int32_t* out = p.out_tokens + size_t(r) * p.out_ld;
+    for (int64_t q = tid; q < p.out_ld; q += kThreads) {
+      int32_t v = -1;
+      if (q < tau) v = p.draft_tokens[p.draft_row0[r] + q];
+      else if (q == tau) v = y;
+      out[q] = v;
     }
-    __syncthreads();
-    int32_t y = red_i[0];
-    __syncthreads();
-    if (y < 0 && rs.resid) {
-      // residual empty to working precision (p and q agree): draw from p with the same uniforms
-      RaceSpec fb = rs;
-      fb.resid = false;
-      float k;
-      race_row_global<E>(fb, trow, nullptr, p.V, red_k, red_i, k, y);
-    }
+  }
+  if (tid == 0) {
+    if (y < 0) report(p.status, SV_ERR_BAD_INPUT);  // the row carries no probability at all
     if (!p.sampler) {
-      int32_t* out = p.out_tokens + size_t(r) * p.out_ld;
-      for (int64_t q = tid; q < p.out_ld; q += kThreads) {
-        int32_t v = -1;
-        if (q < tau) v = p.draft_tokens[p.draft_row0[r] + q];
-        else if (q == tau) v = y;
-        out[q] = v;
-      }
-    }
-    if (tid == 0) {
-      if (y < 0) report(p.status, SV_ERR_BAD_INPUT);  // the row carries no probability at all
-      if (!p.sampler) {
-        p.accepted_len[r] = tau;
-        if (p.correction_token) p.correction_token[r] = y;
-      } else {
-        p.sampled_tokens[sample_row] = y;
-      }
+      p.accepted_len[r] = tau;
+      if (p.correction_token) p.correction_token[r] = y;
+    } else {
+      p.sampled_tokens[sample_row] = y;
     }
   }
-  cluster_sync();  // keep every CTA's shared memory alive until rank 0 has read it
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -663,8 +693,8 @@ struct CommonArgs {
   size_t ws_bytes;
 };
 
-// Race cluster shape for rows of S slices: CL CTAs, each owning every CL-th slice.
-static int32_t race_cluster(int32_t S) { return std::max(1, std::min(kRaceClusterMax, S)); }
+// CTAs per race job for rows of S 16 KB slices: each owns one contiguous share of the row.
+static int32_t race_split(int32_t S) { return std::max(1, std::min(kRaceSplitMax, S)); }
 
 static sv_status check_common(const CommonArgs& a, bool need_target) {
   if (a.dtype != SV_F32 && a.dtype != SV_BF16) return SV_ERR_INVALID;
@@ -701,17 +731,23 @@ static sv_status launch_stream(const StreamParams& sp, cudaStream_t stream) {
 template <typename E>
 static sv_status launch_race(RaceParams rp, int64_t jobs, cudaStream_t stream) {
   if (jobs == 0) return SV_OK;
-  rp.CL = race_cluster(rp.S);
+  rp.CL = race_split(rp.S);
+  // the kernel's share: ceil(V / (CL * kPer)) whole vectors
+  constexpr int64_t kPer = Elem<E>::kPerVec;
+  const int64_t share_bytes = (rp.V + rp.CL * kPer - 1) / (rp.CL * kPer) * 16;
+  rp.stage_share = share_bytes <= int64_t(kRaceShareMax);
+  const size_t smem = rp.stage_share ? size_t(share_bytes) : 0;
+  if (cudaFuncSetAttribute(race_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kRaceShareMax)) != cudaSuccess)
+    return SV_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(jobs * rp.CL));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(rp.CL);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return launch_status(cudaLaunchKernelEx(&cfg, race_kernel<E>, rp));
@@ -748,6 +784,9 @@ static sv_status run_verify(bool block, const CommonArgs& a, const int64_t* targ
   profile_mark(0, stream);
   sv_status st = launch_stream<E>(sp, stream);
   if (st != SV_OK) return st;
+  if (a.gmax == 0 &&  // no stream launch: the race slots are zeroed here instead
+      cudaMemsetAsync(ws.slots, 0, sizeof(RaceSlot) * size_t(a.B), stream) != cudaSuccess)
+    return SV_ERR_CUDA;
 
   DecideParams dp;
   dp.target = sp.target;
@@ -832,7 +871,12 @@ static sv_status run_sample(const CommonArgs& a, const int64_t* draft_row0,
   rp.request_ids = request_ids;
   rp.sampled_tokens = draft_tokens;
   rp.status = status;
-  return launch_race<E>(rp, int64_t(a.B) * a.gmax, stream);
+  rp.ws = verify_layout(a.ws, a.B, a.gmax, chunks_of(a.V, esize<E>()));
+  const int64_t jobs = int64_t(a.B) * a.gmax;
+  if (jobs > 0 &&
+      cudaMemsetAsync(rp.ws.slots, 0, sizeof(RaceSlot) * size_t(jobs), stream) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return launch_race<E>(rp, jobs, stream);
 }
 
 }  // namespace sv

@@ -46,7 +46,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the supplementary rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["markov"], default=None,
+    ap.add_argument("--only", choices=["markov", "schedule"], default=None,
                     help="time one supplementary row alone and print it (profiling runs)")
     ap.add_argument("--markov-positions", type=int, default=None,
                     help="with --only markov: draft this many positions instead of 16")
@@ -401,6 +401,30 @@ def bench_rows(steps, warmup):
     return rows
 
 
+def bench_schedule(steps, warmup):
+    """The scheduler alone on the 512 x 16 workload, each call behind the L2 flush so that the host
+    stays ahead of the GPU."""
+    import torch
+    import speculative_decoding_verification_token_gb300 as sv
+    from speculative_decoding_verification_token_gb300 import synth
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = make_flush(dev)
+    sw = synth.SCHEDULE
+    si = synth.schedule_inputs(sw)
+    c = torch.from_numpy(si["cond_accept"]).to(dev)
+    ml = torch.from_numpy(si["max_len"]).to(dev)
+    sps = torch.from_numpy(si["sps"]).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = {}
+
+    def sch():
+        out["o"] = sv.dspark_schedule(c, ml, sps, si["B_max"], status=status)
+    t = time_calls(sch, steps, warmup, flush, torch.cuda.current_stream())
+    return {"workload": f"{sw.N} requests x {sw.K} positions, B_max={sw.B_max}",
+            "us": sum(t) / len(t) * 1e6, "total_rows": int(out["o"]["total_rows"].item()),
+            "status": int(status.item())}
+
+
 def bench_markov(steps, warmup, flush, stream, positions=None):
     """DSpark Markov-head drafting: 256 requests x 16 positions, V = 151936, R = 256, bf16.  One
     call drafts every position (16 position kernels + 16 select kernels).  Algorithmic bytes per
@@ -477,6 +501,10 @@ def main():
         row = bench_markov(args.steps, args.warmup, make_flush(torch.device("cuda")),
                            torch.cuda.current_stream(), args.markov_positions)
         print(json.dumps({"row": "markov_draft", **row}))
+        return
+    if args.only == "schedule":
+        row = bench_schedule(args.steps, args.warmup)
+        print(json.dumps({"row": "schedule", **row}))
         return
 
     res = bench_token(args, rank, world, peaks, peak_src)

@@ -176,6 +176,22 @@ def make_flush(dev):
     return flush
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x (each rank passes its own); x itself on a single rank."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step, steps, world, max_time):
+    """Units per second over all ranks: every rank (replica) processes units_per_rank_step units
+    per step, and the job takes as long as its slowest rank."""
+    return units_per_rank_step * world * steps / max_time
+
+
 def time_calls(fn, steps, warmup, flush, stream):
     import torch
     for _ in range(warmup):
@@ -234,11 +250,7 @@ def bench_token(args, rank, world, peaks, peak_src):
     nbytes, n_bonus = necessary_bytes(w, acc, esize)
     all_rows_bytes = (2 * w.B * w.gamma + w.B) * w.V * esize
     t_mean = sum(times) / len(times)
-    total_time = sum(times)
-    if world > 1:
-        tt = torch.tensor([total_time], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_time = float(tt.item())
+    total_time = max_over_ranks(sum(times), world, dev)
     res = {
         "w": w, "times": times, "t_mean": t_mean, "total_time": total_time,
         "bytes": nbytes, "all_rows_bytes": all_rows_bytes, "n_bonus": n_bonus,
@@ -509,8 +521,8 @@ def main():
 
     res = bench_token(args, rank, world, peaks, peak_src)
     w = res["w"]
-    value = res["bytes"] * world / res["total_time"] * args.steps / 1e9
-    pos_s = res["positions"] * world * args.steps / res["total_time"]
+    value = whole_job_rate(res["bytes"], args.steps, world, res["total_time"]) / 1e9
+    pos_s = whole_job_rate(res["positions"], args.steps, world, res["total_time"])
     hbm = float(peaks["hbm_gbs"])
     stream_s = res["kernel_ms"][0] * 1e-3
     achieved = res["bytes"] / stream_s / 1e9  # the streaming kernel moves every algorithmic byte

@@ -403,6 +403,17 @@ __device__ __noinline__ void decide_body(const DecideParams& p, int32_t r, bool 
     // row normalisers and the drafted token's ratio, one warp per row
     for (int i = warp + 1; i <= g; i += kWarps) {
       const int32_t unit = r * p.gmax + (i - 1);
+      // lane 0 fetches the drafted token and its two logits while the warp folds the partials
+      const int64_t drow = p.draft_row0[r] + (i - 1);
+      int32_t x = -1;
+      float tx = 0.f, dx = 0.f;
+      if (lane == 0) {
+        x = p.draft_tokens[drow];
+        if (x >= 0 && int64_t(x) < p.V) {
+          tx = Elem<E>::load(row_ptr<E>(p.target, p.target_row0[r] + (i - 1), p.ld), x);
+          dx = Elem<E>::load(row_ptr<E>(p.draft, drow, p.ld), x);
+        }
+      }
       float mt = kM2Empty, st = 0.f, md = kM2Empty, sd = 0.f;
       for (int c = lane; c < p.C; c += 32) {
         const float4 q = __ldcg(&p.ws.partials[size_t(unit) * p.C + c]);
@@ -414,16 +425,11 @@ __device__ __noinline__ void decide_body(const DecideParams& p, int32_t r, bool 
       if (lane == 0) {
         // an all -inf row sums to 0; NaN or +inf logits make the sum NaN
         bool bad = !(st > 0.f && st < INFINITY && sd > 0.f && sd < INFINITY);
-        const int64_t drow = p.draft_row0[r] + (i - 1);
-        const int32_t x = p.draft_tokens[drow];
         float ratio = 0.f;
         if (x < 0 || int64_t(x) >= p.V) {
           bad = true;
         } else {
           // p(x)/q(x) = 2^((t_x log2e - m_t) - (d_x log2e - m_d)) s_d / s_t
-          const float tx =
-              Elem<E>::load(row_ptr<E>(p.target, p.target_row0[r] + (i - 1), p.ld), x);
-          const float dx = Elem<E>::load(row_ptr<E>(p.draft, drow, p.ld), x);
           if (!(dx > -INFINITY)) bad = true;  // q(x) = 0: x cannot have been proposed
           ratio = exp2f(fmaf(tx, kLog2e, -mt) - fmaf(dx, kLog2e, -md)) * (sd / st);
         }

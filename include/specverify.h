@@ -178,7 +178,8 @@ sv_status spec_verify_token_noalloc(const void* target_logits, const void* draft
  * DSpark draft side.
  * ------------------------------------------------------------------------------------------- */
 
-/* Workspace bytes needed by dspark_markov_draft. */
+/* Workspace bytes needed by dspark_markov_draft: one race partial per (request, CTA) and a
+ * [K][B] table of published race bounds; 0 for sizes the call rejects. */
 size_t dspark_markov_workspace_bytes(int32_t B, int32_t K, int64_t V, int32_t R);
 
 /* Markov-head drafting ("DeepSeek DSpark 详解" §03; "How much does a token cost", "DSpark

@@ -9,10 +9,12 @@
 //                           backbone tile (128 requests x 64 columns) into a two-stage ring;
 //               warp 1      tcgen05.mma (M = 128, N = 64, K = 256) into one of two TMEM
 //                           accumulators;
-//               warps 2-9   the epilogue: TMEM -> registers, + backbone, round to bf16, TMA store
-//                           of z, and per request: log2-domain softmax statistics and the
-//                           exponential race x_k = argmax z - log(-log u) (DRAFT tag, position k)
-//                           behind a noise gate, written as one partial per (request, CTA).
+//               warps 2-17  the epilogue, 16 columns of 32 requests per warp and tile: TMEM ->
+//                           registers, + backbone, round to bf16, a per-warp TMA store of z, and
+//                           per request: log2-domain softmax statistics and the exponential race
+//                           x_k = argmax z - log(-log u) (DRAFT tag, position k) behind a noise
+//                           gate whose bound is shared by every CTA of the row through a global
+//                           table; one partial per (request, CTA).
 //   select    folds the partials of every request into x_k, the row statistics of z_k and the
 //             sequential-temperature-scaled confidence conf_k = 1 / (1 + exp(-s_k / T_k)).
 #include <algorithm>
@@ -36,8 +38,9 @@ constexpr int kMkThreads = 32 * (2 + kMkEpiWarps);
 constexpr uint32_t kMkABytes = kMkKB * kMkRows * 128;     // 64 KB
 constexpr uint32_t kMkBBytes = kMkKB * kMkCols * 128;     // 32 KB per stage
 constexpr uint32_t kMkBBBytes = kMkRows * 128;            // 16 KB per stage (64 bf16 per row)
-constexpr uint32_t kMkZBytes = kMkRows * 128;             // 16 KB per z staging buffer
-constexpr size_t kMkSmem = 1024 + kMkABytes + kMkStages * (kMkBBytes + kMkBBBytes) + 2 * kMkZBytes;
+constexpr uint32_t kMkZWarpBytes = 32 * 32;               // one warp's z block: 32 rows x 16 bf16
+constexpr uint32_t kMkZBytes = 2 * kMkEpiWarps * kMkZWarpBytes;  // double-buffered, 32 KB
+constexpr size_t kMkSmem = 1024 + kMkABytes + kMkStages * (kMkBBytes + kMkBBBytes) + kMkZBytes;
 constexpr uint32_t kMkTmemCols = 2 * kMkCols;             // two accumulators
 
 struct MkPartial {  // one (request, CTA) partial of position k
@@ -60,6 +63,7 @@ struct MkParams {
   const uint64_t* request_ids;
   int32_t write_z;
   MkPartial* partials;        // [B][per_mblock]
+  uint32_t* k0;               // [B] best exact race key published for row b so far (key_order; 0: none)
   int32_t* status;
 };
 
@@ -72,20 +76,17 @@ struct KeyIdx {
   int32_t idx;
 };
 
-// Exact race keys of the entries flagged in `surv` (bit j: column c0 + j of this thread's quarter)
-// against the running best; their z is read back from the staged tile row `zrow` (two 16-byte
-// chunks of the 128-byte swizzled row r, chunk index cq and cq + 1).  Rare: out of line.
+// Exact race keys of the entries flagged in `surv` (bit j: column c0 + j of this thread's 16
+// columns) against the running best; their z is read back from the thread's staged bf16 row
+// `zrow`.  Rare: out of line.
 __device__ __noinline__ KeyIdx markov_survivors(Stream st, uint32_t surv, int64_t c0, int64_t V,
-                                                const uint8_t* tile, uint32_t r, uint32_t cq,
-                                                KeyIdx best) {
+                                                const uint16_t* zrow, KeyIdx best) {
   while (surv) {
     const uint32_t j = __ffs(surv) - 1;
     surv &= surv - 1;
     const int64_t e = c0 + j;
     if (e >= V) continue;
-    const uint16_t zbits =
-        *reinterpret_cast<const uint16_t*>(tile + tc::sw128(r, cq + (j >> 3)) + 2 * (j & 7));
-    const float z = __uint_as_float(uint32_t(zbits) << 16);
+    const float z = __uint_as_float(uint32_t(zrow[j]) << 16);
     if (!(z > -INFINITY)) continue;
     const uint4 blk = stream_block(st, static_cast<uint32_t>(e >> 2));
     const float key = z + race_noise(uniform_of(word_of(blk, j & 3)));
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = sA + kMkABytes;                          // [stage][kb] 8 KB tiles
   uint8_t* sBB = sB + kMkStages * kMkBBytes;             // [stage] 16 KB
-  uint8_t* sZ = sBB + kMkStages * kMkBBBytes;            // [2] 16 KB
+  uint8_t* sZ = sBB + kMkStages * kMkBBBytes;            // [warp][2] 1 KB
   __shared__ uint64_t b_full[kMkStages], b_empty[kMkStages];
   __shared__ uint64_t bb_full[kMkStages], bb_empty[kMkStages];
   __shared__ uint64_t acc_full[2], acc_empty[2];
@@ -234,9 +235,15 @@ __global__ void __launch_bounds__(kMkThreads, 1)
     const int h = (warp - 2) >> 2;
     const uint32_t r = 32 * q + lane;
     const int32_t b = m0 + static_cast<int32_t>(r);
-    const bool issuer = tid == 64;  // issues the z stores
     const uint64_t req = b < p.B ? (p.request_ids ? p.request_ids[b] : uint64_t(b)) : 0;
     const Stream st = make_stream(p.seed, req, static_cast<uint32_t>(p.k), kTagDraft);
+    // Row-wide race bound: every CTA that holds a column range of row b publishes its best exact
+    // key there, and every thread gates its entries against the largest key published so far
+    // (read one tile late, off the critical path).  Any published key is the key of an entry of
+    // the row, so it never exceeds the row's maximum and the gate stays conservative.
+    uint32_t* const kslot = b < p.B ? p.k0 + b : nullptr;
+    uint32_t kpub = 0;            // key_order of the published bound read at the previous tile
+    float published = -INFINITY;  // the largest key this thread has published
     float m2 = kM2Empty, s = 0.f, zmax = -INFINITY;
     KeyIdx best = {-INFINITY, -1};
     bool failed = false;
@@ -262,13 +269,17 @@ __global__ void __launch_bounds__(kMkThreads, 1)
       const int valid = static_cast<int>(p.V - c0 < 16 ? (p.V - c0 > 0 ? p.V - c0 : 0) : 16);
       uint32_t zp[8];
       markov_round(v, bb0, bb1, valid, zp);
-      // stage the z tile: source of the TMA store and of the survivors' re-read.  Buffer t & 1 was
-      // last read by the store of tile t - 2, which finished reading before the barrier of tile
-      // t - 1 (the issuer waits for it there).
-      uint8_t* zt = sZ + (t & 1) * kMkZBytes;
-      *reinterpret_cast<uint4*>(zt + tc::sw128(r, 2 * h)) = make_uint4(zp[0], zp[1], zp[2], zp[3]);
-      *reinterpret_cast<uint4*>(zt + tc::sw128(r, 2 * h + 1)) =
-          make_uint4(zp[4], zp[5], zp[6], zp[7]);
+      // stage this warp's 32 x 16 block of z: the source of its TMA store and of the survivors'
+      // re-read.  Buffer t & 1 was last read by the warp's store of tile t - 2; lane 0 lets at
+      // most the store of tile t - 1 still be reading.
+      uint8_t* zt = sZ + ((warp - 2) * 2 + (t & 1)) * kMkZWarpBytes;
+      const uint16_t* zrow = reinterpret_cast<const uint16_t*>(zt + 32 * lane);
+      if (p.write_z) {
+        if (lane == 0) tc::bulk_wait_read<1>();
+        __syncwarp();
+      }
+      *reinterpret_cast<uint4*>(zt + 32 * lane) = make_uint4(zp[0], zp[1], zp[2], zp[3]);
+      *reinterpret_cast<uint4*>(zt + 32 * lane + 16) = make_uint4(zp[4], zp[5], zp[6], zp[7]);
       // softmax statistics (log2 domain): one rescale per tile, then e_j = 2^(z_j log2e - m2)
       float tmax = -INFINITY;
 #pragma unroll
@@ -288,8 +299,8 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         for (int j = 0; j < 8; ++j) part[j] = e[j] + e[j + 8];
         s += ((part[0] + part[4]) + (part[2] + part[6])) + ((part[1] + part[5]) + (part[3] + part[7]));
       }
-      // exponential race, key z_j + G_j with G_j = -log(-log u_j).  Entry j can reach the
-      // running best K only if G_j >= K - z_j; since G <= -log(1 - u) and
+      // exponential race, key z_j + G_j with G_j = -log(-log u_j).  K is the larger of this
+      // thread's best key and the row bound.  Entry j can reach K only if G_j >= K - z_j; since G <= -log(1 - u) and
       // 1 - u > ((~w) >> 9) 2^-23, that needs ((~w) >> 9) <= 2^((z_j - K) log2e + 23)
       // = e_j 2^(m2 + 23 - K log2e).  The 1e-3 margin covers the binary32 rounding of both
       // sides; the few entries that pass are keyed exactly (markov_survivors).
@@ -299,9 +310,11 @@ __global__ void __launch_bounds__(kMkThreads, 1)
           uint32_t top = 0;
 #pragma unroll
           for (int j = 0; j < 16; ++j) top |= (v[j] == tmax ? 1u : 0u) << j;
-          best = markov_survivors(st, top, c0, p.V, zt, r, 2 * h, best);
+          best = markov_survivors(st, top, c0, p.V, zrow, best);
         }
-        const float C = fast_exp2(m2 + 23.0f - best.key * kLog2e) * 1.001f;
+        const float kp = key_from_order(kpub);
+        const float K = fmaxf(best.key, kp);
+        const float C = fast_exp2(m2 + 23.0f - K * kLog2e) * 1.001f;
         // rej collects, most significant first, the sign of e_j C - ((~w) >> 9): set = rejected
         // (fma rounds the exact difference once, so its sign is exact)
         uint32_t rej = 0;
@@ -316,14 +329,20 @@ __global__ void __launch_bounds__(kMkThreads, 1)
           }
         }
         const uint32_t surv = __brev(~rej) >> 16;  // bit j: entry j may beat K
-        if (surv) best = markov_survivors(st, surv, c0, p.V, zt, r, 2 * h, best);
+        if (surv) best = markov_survivors(st, surv, c0, p.V, zrow, best);
+        if (kslot) {
+          if (best.key > published && best.key > kp) {
+            atomicMax(kslot, key_order(best.key));
+            published = best.key;
+          }
+          kpub = __ldcg(kslot);  // consumed at the next tile
+        }
       }
       if (p.write_z) {
         fence_proxy_async();
-        if (issuer) tc::bulk_wait_read<0>();  // the store of tile t - 1 has read its buffer
-        named_sync(1, 32 * kMkEpiWarps);
-        if (issuer) {
-          tc::tma_store_3d(&map_z, zt, n * kMkCols, p.k - 1, m0);
+        __syncwarp();
+        if (lane == 0 && valid > 0 && m0 + 32 * q < p.B) {  // boxes past V or B: nothing to store
+          tc::tma_store_3d(&map_z, zt, static_cast<int32_t>(c0), p.k - 1, m0 + 32 * q);
           tc::bulk_commit();
         }
       }
@@ -357,7 +376,7 @@ __global__ void __launch_bounds__(kMkThreads, 1)
       out.pad[0] = out.pad[1] = out.pad[2] = 0;
       p.partials[size_t(b) * p.per_mblock + ci] = out;
     }
-    if (issuer) tc::bulk_wait_all();
+    if (lane == 0) tc::bulk_wait_all();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -430,7 +449,8 @@ EncodeTiledFn encode_tiled() {
 // bf16 tensor map with 128-byte swizzle; dims[0] is the contiguous one, strides in bytes for
 // dims 1.. ; out-of-range elements load as zero and are skipped by stores.
 bool make_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-              const uint64_t* strides, const uint32_t* box) {
+              const uint64_t* strides, const uint32_t* box,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
   cuuint64_t d[3], st[2];
@@ -441,7 +461,7 @@ bool make_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims
   }
   for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, bx, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -459,19 +479,23 @@ bool markov_geom(int32_t B, int64_t V, MkGeom* g) {
   return true;
 }
 
-size_t markov_ws_bytes(int32_t B, const MkGeom& g) {
+// [B][per_mblock] partials, then the [K][B] published race bounds
+size_t markov_partials_bytes(int32_t B, const MkGeom& g) {
   return (size_t(B) * g.per_mblock * sizeof(MkPartial) + 255) & ~size_t(255);
+}
+
+size_t markov_ws_bytes(int32_t B, int32_t K, const MkGeom& g) {
+  return markov_partials_bytes(B, g) + ((size_t(K) * B * sizeof(uint32_t) + 255) & ~size_t(255));
 }
 
 }  // namespace
 }  // namespace sv
 
 extern "C" size_t dspark_markov_workspace_bytes(int32_t B, int32_t K, int64_t V, int32_t R) {
-  (void)K;
   (void)R;
   sv::MkGeom g;
-  if (B <= 0 || V <= 0 || !sv::markov_geom(B, V, &g)) return 0;
-  return sv::markov_ws_bytes(B, g);
+  if (B <= 0 || K < 1 || V <= 0 || !sv::markov_geom(B, V, &g)) return 0;
+  return sv::markov_ws_bytes(B, K, g);
 }
 
 extern "C" sv_status dspark_markov_draft(const void* backbone_logits, int64_t ldb, const void* U,
@@ -499,7 +523,7 @@ extern "C" sv_status dspark_markov_draft(const void* backbone_logits, int64_t ld
   if (B == 0) return SV_OK;
   MkGeom g;
   if (!markov_geom(B, V, &g)) return SV_ERR_CUDA;
-  if (!workspace || !aligned256(workspace) || workspace_bytes < markov_ws_bytes(B, g))
+  if (!workspace || !aligned256(workspace) || workspace_bytes < markov_ws_bytes(B, K, g))
     return SV_ERR_INVALID;
 
   // tensor maps: Wt [V][R]; backbone and z [B][K][V] with row (b, k) at (b K + k) ld elements
@@ -519,8 +543,9 @@ extern "C" sv_status dspark_markov_draft(const void* backbone_logits, int64_t ld
   if (draft_logits_out) {
     const uint64_t dims[3] = {uint64_t(V), uint64_t(K), uint64_t(B)};
     const uint64_t strides[2] = {uint64_t(ldz) * 2, uint64_t(ldz) * 2 * K};
-    const uint32_t box[3] = {kMkCols, 1, kMkRows};
-    if (!make_map(&map_z, draft_logits_out, 3, dims, strides, box)) return SV_ERR_CUDA;
+    const uint32_t box[3] = {16, 1, 32};  // one epilogue warp's block, stored unswizzled
+    if (!make_map(&map_z, draft_logits_out, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return SV_ERR_CUDA;
   } else {
     map_z = map_bb;  // never used: write_z = 0
   }
@@ -542,12 +567,17 @@ extern "C" sv_status dspark_markov_draft(const void* backbone_logits, int64_t ld
   p.request_ids = request_ids;
   p.write_z = draft_logits_out != nullptr;
   p.partials = static_cast<MkPartial*>(workspace);
+  uint32_t* const bounds = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) +
+                                                       markov_partials_bytes(B, g));
   p.status = status;
   const int grid = g.n_mblocks * g.per_mblock;
   const int sel_grid = (B + 7) / 8;
+  if (cudaMemsetAsync(bounds, 0, size_t(K) * B * sizeof(uint32_t), cs) != cudaSuccess)
+    return SV_ERR_CUDA;
   profile_mark(0, cs);
   for (int32_t k = 1; k <= K; ++k) {
     p.k = k;
+    p.k0 = bounds + size_t(k - 1) * B;
     markov_position_kernel<0><<<grid, kMkThreads, kMkSmem, cs>>>(map_wt, map_bb, map_z, p);
     if (k == 1) profile_mark(1, cs);
     markov_select_kernel<<<sel_grid, 256, 0, cs>>>(p.partials, g.per_mblock, B, K, k, conf_scores,

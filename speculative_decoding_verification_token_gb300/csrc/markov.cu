@@ -10,11 +10,14 @@
 //               warp 1      tcgen05.mma (M = 128, N = 64, K = 256) into one of two TMEM
 //                           accumulators;
 //               warps 2-17  the epilogue, 16 columns of 32 requests per warp and tile: TMEM ->
-//                           registers, + backbone, round to bf16, a per-warp TMA store of z, and
+//                           registers, + backbone, round to bf16 and staged in shared memory
+//                           (three tiles deep), and
 //                           per request: log2-domain softmax statistics and the exponential race
 //                           x_k = argmax z - log(-log u) (DRAFT tag, position k) behind a noise
 //                           gate whose bound is shared by every CTA of the row through a global
 //                           table; one partial per (request, CTA).
+//               warp 18     TMA stores of the staged z, one per lane quadrant (32 requests x
+//                           64 columns) and tile.
 //   select    folds the partials of every request into x_k, the row statistics of z_k and the
 //             sequential-temperature-scaled confidence conf_k = 1 / (1 + exp(-s_k / T_k)).
 #include <algorithm>
@@ -34,12 +37,14 @@ constexpr int kMkRank = 256;                 // R (UMMA K)
 constexpr int kMkKB = kMkRank / 64;          // 128-byte k-blocks per row
 constexpr int kMkStages = 2;                 // Wt / backbone ring depth
 constexpr int kMkEpiWarps = 16;            // 4 lane quadrants x 4 column quarters
-constexpr int kMkThreads = 32 * (2 + kMkEpiWarps);
+constexpr int kMkStoreWarp = 2 + kMkEpiWarps;       // issues the z stores
+constexpr int kMkThreads = 32 * (3 + kMkEpiWarps);
+constexpr int kMkZBufs = 3;                          // z staging depth (tiles)
 constexpr uint32_t kMkABytes = kMkKB * kMkRows * 128;     // 64 KB
 constexpr uint32_t kMkBBytes = kMkKB * kMkCols * 128;     // 32 KB per stage
 constexpr uint32_t kMkBBBytes = kMkRows * 128;            // 16 KB per stage (64 bf16 per row)
-constexpr uint32_t kMkZWarpBytes = 32 * 32;               // one warp's z block: 32 rows x 16 bf16
-constexpr uint32_t kMkZBytes = 2 * kMkEpiWarps * kMkZWarpBytes;  // double-buffered, 32 KB
+constexpr uint32_t kMkZGroupBytes = 32 * 128;             // a lane quadrant's z block: 32 x 64 bf16
+constexpr uint32_t kMkZBytes = kMkZBufs * 4 * kMkZGroupBytes;  // [buffer][quadrant]: 48 KB
 constexpr size_t kMkSmem = 1024 + kMkABytes + kMkStages * (kMkBBytes + kMkBBBytes) + kMkZBytes;
 constexpr uint32_t kMkTmemCols = 2 * kMkCols;             // two accumulators
 
@@ -77,16 +82,19 @@ struct KeyIdx {
 };
 
 // Exact race keys of the entries flagged in `surv` (bit j: column c0 + j of this thread's 16
-// columns) against the running best; their z is read back from the thread's staged bf16 row
-// `zrow`.  Rare: out of line.
+// columns) against the running best; their z is read back from the staged block `tile` (two
+// 16-byte chunks, cq and cq + 1, of the 128-byte swizzled row r).  Rare: out of line.
 __device__ __noinline__ KeyIdx markov_survivors(Stream st, uint32_t surv, int64_t c0, int64_t V,
-                                                const uint16_t* zrow, KeyIdx best) {
+                                                const uint8_t* tile, uint32_t r, uint32_t cq,
+                                                KeyIdx best) {
   while (surv) {
     const uint32_t j = __ffs(surv) - 1;
     surv &= surv - 1;
     const int64_t e = c0 + j;
     if (e >= V) continue;
-    const float z = __uint_as_float(uint32_t(zrow[j]) << 16);
+    const uint16_t zbits =
+        *reinterpret_cast<const uint16_t*>(tile + tc::sw128(r, cq + (j >> 3)) + 2 * (j & 7));
+    const float z = __uint_as_float(uint32_t(zbits) << 16);
     if (!(z > -INFINITY)) continue;
     const uint4 blk = stream_block(st, static_cast<uint32_t>(e >> 2));
     const float key = z + race_noise(uniform_of(word_of(blk, j & 3)));
@@ -132,10 +140,11 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = sA + kMkABytes;                          // [stage][kb] 8 KB tiles
   uint8_t* sBB = sB + kMkStages * kMkBBytes;             // [stage] 16 KB
-  uint8_t* sZ = sBB + kMkStages * kMkBBBytes;            // [warp][2] 1 KB
+  uint8_t* sZ = sBB + kMkStages * kMkBBBytes;            // [buffer][quadrant] 4 KB
   __shared__ uint64_t b_full[kMkStages], b_empty[kMkStages];
   __shared__ uint64_t bb_full[kMkStages], bb_empty[kMkStages];
   __shared__ uint64_t acc_full[2], acc_empty[2];
+  __shared__ uint64_t z_full[kMkZBufs], z_empty[kMkZBufs];
   __shared__ uint32_t tmem_base;
   __shared__ float merge[3][kMkRows][5];  // column quarters 1..3 -> quarter 0
   __shared__ int32_t s_bad;
@@ -157,6 +166,10 @@ __global__ void __launch_bounds__(kMkThreads, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], kMkEpiWarps);
+    }
+    for (int z = 0; z < kMkZBufs; ++z) {
+      mbar_init(&z_full[z], kMkEpiWarps);
+      mbar_init(&z_empty[z], 1);
     }
     fence_barrier_init();
   }
@@ -228,6 +241,25 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         tc::mma_commit(&acc_full[acc]);
       }
     }
+  } else if (warp == kMkStoreWarp) {
+    // ---- z stores: once the sixteen epilogue warps have staged tile t in buffer t % kMkZBufs,
+    // store its four 32 x 64 quadrant blocks; once the stores of tile t - 1 have read their
+    // buffer, hand that buffer back to the epilogue
+    if (lane == 0 && p.write_z) {
+      for (int t = 0; t < n_my; ++t) {
+        const int32_t n = ci + t * p.per_mblock;
+        const int zb = t % kMkZBufs;
+        if (!mbar_wait(&z_full[zb], (t / kMkZBufs) & 1, p.status)) break;
+        for (int q = 0; q < 4; ++q)
+          if (m0 + 32 * q < p.B)  // a block wholly past B has nothing to store
+            tc::tma_store_3d(&map_z, sZ + (zb * 4 + q) * kMkZGroupBytes, n * kMkCols, p.k - 1,
+                             m0 + 32 * q);
+        tc::bulk_commit();
+        tc::bulk_wait_read<1>();
+        if (t > 0) mbar_arrive(&z_empty[(t - 1) % kMkZBufs]);
+      }
+      tc::bulk_wait_all();
+    }
   } else {
     // ---- epilogue: warp w reads TMEM lane quadrant q = w % 4 (rows 32q .. 32q + 31) and column
     // quarter h (16 columns) of each 64-column tile; thread (q, lane) owns request m0 + 32q + lane.
@@ -269,17 +301,18 @@ __global__ void __launch_bounds__(kMkThreads, 1)
       const int valid = static_cast<int>(p.V - c0 < 16 ? (p.V - c0 > 0 ? p.V - c0 : 0) : 16);
       uint32_t zp[8];
       markov_round(v, bb0, bb1, valid, zp);
-      // stage this warp's 32 x 16 block of z: the source of its TMA store and of the survivors'
-      // re-read.  Buffer t & 1 was last read by the warp's store of tile t - 2; lane 0 lets at
-      // most the store of tile t - 1 still be reading.
-      uint8_t* zt = sZ + ((warp - 2) * 2 + (t & 1)) * kMkZWarpBytes;
-      const uint16_t* zrow = reinterpret_cast<const uint16_t*>(zt + 32 * lane);
-      if (p.write_z) {
-        if (lane == 0) tc::bulk_wait_read<1>();
+      // stage the quadrant's 32 x 64 block of z (the four warps of lane quadrant q, one 16-column
+      // quarter each): the source of its TMA store and of the survivors' re-read.  The buffer was
+      // last read by the stores of tile t - kMkZBufs.
+      const int zb = t % kMkZBufs;
+      uint8_t* zt = sZ + (zb * 4 + q) * kMkZGroupBytes;
+      if (p.write_z && t >= kMkZBufs) {
+        if (!failed && !mbar_wait(&z_empty[zb], (t / kMkZBufs - 1) & 1, p.status)) failed = true;
         __syncwarp();
       }
-      *reinterpret_cast<uint4*>(zt + 32 * lane) = make_uint4(zp[0], zp[1], zp[2], zp[3]);
-      *reinterpret_cast<uint4*>(zt + 32 * lane + 16) = make_uint4(zp[4], zp[5], zp[6], zp[7]);
+      *reinterpret_cast<uint4*>(zt + tc::sw128(lane, 2 * h)) = make_uint4(zp[0], zp[1], zp[2], zp[3]);
+      *reinterpret_cast<uint4*>(zt + tc::sw128(lane, 2 * h + 1)) =
+          make_uint4(zp[4], zp[5], zp[6], zp[7]);
       // softmax statistics (log2 domain): one rescale per tile, then e_j = 2^(z_j log2e - m2)
       float tmax = -INFINITY;
 #pragma unroll
@@ -310,7 +343,7 @@ __global__ void __launch_bounds__(kMkThreads, 1)
           uint32_t top = 0;
 #pragma unroll
           for (int j = 0; j < 16; ++j) top |= (v[j] == tmax ? 1u : 0u) << j;
-          best = markov_survivors(st, top, c0, p.V, zrow, best);
+          best = markov_survivors(st, top, c0, p.V, zt, lane, 2 * h, best);
         }
         const float kp = key_from_order(kpub);
         const float K = fmaxf(best.key, kp);
@@ -329,7 +362,7 @@ __global__ void __launch_bounds__(kMkThreads, 1)
           }
         }
         const uint32_t surv = __brev(~rej) >> 16;  // bit j: entry j may beat K
-        if (surv) best = markov_survivors(st, surv, c0, p.V, zrow, best);
+        if (surv) best = markov_survivors(st, surv, c0, p.V, zt, lane, 2 * h, best);
         if (kslot) {
           if (best.key > published && best.key > kp) {
             atomicMax(kslot, key_order(best.key));
@@ -339,12 +372,9 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         }
       }
       if (p.write_z) {
-        fence_proxy_async();
+        fence_proxy_async();  // the staged block is read by the async proxy (TMA store)
         __syncwarp();
-        if (lane == 0 && valid > 0 && m0 + 32 * q < p.B) {  // boxes past V or B: nothing to store
-          tc::tma_store_3d(&map_z, zt, static_cast<int32_t>(c0), p.k - 1, m0 + 32 * q);
-          tc::bulk_commit();
-        }
+        if (lane == 0) mbar_arrive(&z_full[zb]);
       }
     }
     // fold the four column quarters of every request and publish this CTA's partial
@@ -376,7 +406,6 @@ __global__ void __launch_bounds__(kMkThreads, 1)
       out.pad[0] = out.pad[1] = out.pad[2] = 0;
       p.partials[size_t(b) * p.per_mblock + ci] = out;
     }
-    if (lane == 0) tc::bulk_wait_all();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -543,9 +572,8 @@ extern "C" sv_status dspark_markov_draft(const void* backbone_logits, int64_t ld
   if (draft_logits_out) {
     const uint64_t dims[3] = {uint64_t(V), uint64_t(K), uint64_t(B)};
     const uint64_t strides[2] = {uint64_t(ldz) * 2, uint64_t(ldz) * 2 * K};
-    const uint32_t box[3] = {16, 1, 32};  // one epilogue warp's block, stored unswizzled
-    if (!make_map(&map_z, draft_logits_out, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
-      return SV_ERR_CUDA;
+    const uint32_t box[3] = {kMkCols, 1, 32};  // one lane quadrant's block
+    if (!make_map(&map_z, draft_logits_out, 3, dims, strides, box)) return SV_ERR_CUDA;
   } else {
     map_z = map_bb;  // never used: write_z = 0
   }

@@ -111,14 +111,13 @@ __device__ __noinline__ KeyIdx markov_survivors(Stream st, uint32_t surv, int64_
 // on to -inf: they hold zero-filled operands.
 __device__ __forceinline__ void markov_round(float* v, const uint4& bb0, const uint4& bb1,
                                              int valid, uint32_t* zp) {
-  float bb[16];
-  Elem<bf16_tag>::unpack(bb0, bb);
-  Elem<bf16_tag>::unpack(bb1, bb + 8);
+  const uint32_t bw[8] = {bb0.x, bb0.y, bb0.z, bb0.w, bb1.x, bb1.y, bb1.z, bb1.w};
 #pragma unroll
   for (int j = 0; j < 16; j += 2) {
-    const __nv_bfloat162 z2 = __floats2bfloat162_rn(v[j] + bb[j], v[j + 1] + bb[j + 1]);
+    const float2 zs = add2(make_float2(v[j], v[j + 1]), bf16x2_f2(bw[j / 2]));
+    const __nv_bfloat162 z2 = __float22bfloat162_rn(zs);
     zp[j / 2] = *reinterpret_cast<const uint32_t*>(&z2);
-    const float2 zf = __bfloat1622float2(z2);
+    const float2 zf = bf16x2_f2(zp[j / 2]);
     v[j] = zf.x;
     v[j + 1] = zf.y;
   }
@@ -323,14 +322,14 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         s *= fast_exp2(m2 - vm);
         m2 = vm;
       }
-      float e[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) e[j] = fast_exp2(fmaf(v[j], kLog2e, -m2));
+      float2 e[8];  // e[i] = (e_{2i}, e_{2i+1})
       {
-        float part[8];
+        const float2 l2 = splat2(kLog2e), nm = splat2(-m2);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) part[j] = e[j] + e[j + 8];
-        s += ((part[0] + part[4]) + (part[2] + part[6])) + ((part[1] + part[5]) + (part[3] + part[7]));
+        for (int i = 0; i < 8; ++i) e[i] = exp2_2(fma2(make_float2(v[2 * i], v[2 * i + 1]), l2, nm));
+        const float2 t = add2(add2(add2(e[0], e[4]), add2(e[2], e[6])),
+                              add2(add2(e[1], e[5]), add2(e[3], e[7])));
+        s += t.x + t.y;
       }
       // exponential race, key z_j + G_j with G_j = -log(-log u_j).  K is the larger of this
       // thread's best key and the row bound.  Entry j can reach K only if G_j >= K - z_j; since G <= -log(1 - u) and
@@ -351,14 +350,20 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         // rej collects, most significant first, the sign of e_j C - ((~w) >> 9): set = rejected
         // (fma rounds the exact difference once, so its sign is exact)
         uint32_t rej = 0;
+        const float2 C2 = splat2(C);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const uint4 blk = stream_block(st, static_cast<uint32_t>((c0 >> 2) + g));
           const uint32_t w4[4] = {blk.x, blk.y, blk.z, blk.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float mf = __uint_as_float((w4[j] >> 9) ^ 0x4B7FFFFFu) - 8388608.0f;
-            rej = __funnelshift_l(__float_as_uint(fmaf(e[4 * g + j], C, -mf)), rej, 1);
+          for (int j = 0; j < 4; j += 2) {
+            // -((~w) >> 9) as binary32, for two entries: -(2^23 + that integer), plus 2^23
+            const float2 nmf = add2(make_float2(__uint_as_float((w4[j] >> 9) ^ 0xCB7FFFFFu),
+                                                __uint_as_float((w4[j + 1] >> 9) ^ 0xCB7FFFFFu)),
+                                    splat2(8388608.0f));
+            const float2 d = fma2(e[2 * g + j / 2], C2, nmf);
+            rej = __funnelshift_l(__float_as_uint(d.x), rej, 1);
+            rej = __funnelshift_l(__float_as_uint(d.y), rej, 1);
           }
         }
         const uint32_t surv = __brev(~rej) >> 16;  // bit j: entry j may beat K

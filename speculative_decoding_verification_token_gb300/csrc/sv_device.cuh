@@ -319,8 +319,21 @@ __device__ __forceinline__ void ms2_vec_f32(float& m, float& s, const uint4& v) 
   ms2_fold(m, s, x, vmax, 4);
 }
 
+// ---- packed binary32 pairs: one fma / add instruction for two lanes, each rounded exactly as the
+// scalar operation would be
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
+// a packed bf16 pair (low half first) widened to binary32, exactly
+__device__ __forceinline__ float2 bf16x2_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ float2 exp2_2(float2 a) {
+  return make_float2(fast_exp2(a.x), fast_exp2(a.y));
+}
+
 // Fold N 16-byte vectors into (m, s): one maximum over all of them decides a (rare) rescale, then
-// every element costs one fma, one ex2 and one add (the vector's eight summed as a tree).
+// every element costs half a packed fma, one ex2 and half a packed add (summed as a tree).
 template <int N>
 __device__ __forceinline__ void ms2_fold_vecs_bf16(float& m, float& s, const uint4* v) {
   auto pair = [](uint32_t w) { return *reinterpret_cast<const __nv_bfloat162*>(&w); };
@@ -334,16 +347,17 @@ __device__ __forceinline__ void ms2_fold_vecs_bf16(float& m, float& s, const uin
     s *= fast_exp2(m - vm);
     m = vm;
   }
-  float tot = 0.f;
+  const float2 l2 = splat2(kLog2e), nm = splat2(-m);
+  float2 tot = make_float2(0.f, 0.f);
 #pragma unroll
   for (int u = 0; u < N; ++u) {
-    float x[8], e[8];
-    Elem<bf16_tag>::unpack(v[u], x);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) e[j] = fast_exp2(fmaf(x[j], kLog2e, -m));
-    tot += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+    const float2 e0 = exp2_2(fma2(bf16x2_f2(v[u].x), l2, nm));
+    const float2 e1 = exp2_2(fma2(bf16x2_f2(v[u].y), l2, nm));
+    const float2 e2 = exp2_2(fma2(bf16x2_f2(v[u].z), l2, nm));
+    const float2 e3 = exp2_2(fma2(bf16x2_f2(v[u].w), l2, nm));
+    tot = add2(tot, add2(add2(e0, e1), add2(e2, e3)));
   }
-  s += tot;
+  s += tot.x + tot.y;
 }
 
 template <int N>
@@ -358,16 +372,15 @@ __device__ __forceinline__ void ms2_fold_vecs_f32(float& m, float& s, const uint
     s *= fast_exp2(m - vm);
     m = vm;
   }
-  float tot = 0.f;
+  const float2 l2 = splat2(kLog2e), nm = splat2(-m);
+  float2 tot = make_float2(0.f, 0.f);
 #pragma unroll
   for (int u = 0; u < N; ++u) {
-    const float e0 = fast_exp2(fmaf(__uint_as_float(v[u].x), kLog2e, -m));
-    const float e1 = fast_exp2(fmaf(__uint_as_float(v[u].y), kLog2e, -m));
-    const float e2 = fast_exp2(fmaf(__uint_as_float(v[u].z), kLog2e, -m));
-    const float e3 = fast_exp2(fmaf(__uint_as_float(v[u].w), kLog2e, -m));
-    tot += (e0 + e1) + (e2 + e3);
+    const float2 e0 = exp2_2(fma2(make_float2(__uint_as_float(v[u].x), __uint_as_float(v[u].y)), l2, nm));
+    const float2 e1 = exp2_2(fma2(make_float2(__uint_as_float(v[u].z), __uint_as_float(v[u].w)), l2, nm));
+    tot = add2(tot, add2(e0, e1));
   }
-  s += tot;
+  s += tot.x + tot.y;
 }
 
 __device__ __forceinline__ void ms2_one(float& m, float& s, float x) {

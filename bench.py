@@ -46,7 +46,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the supplementary rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["markov", "schedule"], default=None,
+    ap.add_argument("--only", choices=["markov", "schedule", "block"], default=None,
                     help="time one supplementary row alone and print it (profiling runs)")
     ap.add_argument("--markov-positions", type=int, default=None,
                     help="with --only markov: draft this many positions instead of 16")
@@ -346,28 +346,7 @@ def bench_rows(steps, warmup):
     stream = torch.cuda.current_stream()
     flush = make_flush(dev)
     rows = {}
-    # block verification, 128 requests x 7, V = 129280
-    w = synth.BLOCK_LARGE
-    inp = synth.token_inputs(w, device=dev)
-    tokens = sv.spec_sample_draft(inp["draft"], inp["draft_row0"], inp["draft_len"], w.gamma,
-                                  w.seed)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws = sv.workspace(sv.spec_verify_workspace_bytes(w.B, w.gamma, w.V, sv.SV_BF16), dev)
-    holder = {}
-
-    def blk():
-        holder["o"] = sv.spec_verify_block(inp["target"], inp["draft"], inp["target_row0"],
-                                           inp["draft_row0"], inp["draft_len"], w.gamma, tokens,
-                                           w.seed, status=status, workspace=ws)
-    t = time_calls(blk, steps, warmup, flush, stream)
-    acc = holder["o"]["accepted_len"].cpu()
-    n_bonus = int((acc == w.gamma).sum())
-    nb = (2 * w.B * w.gamma + n_bonus) * w.V * 2
-    tm = sum(t) / len(t)
-    rows["block_verify_128x7_V129280_bf16"] = {
-        "ms": tm * 1e3, "GB_s": nb / tm / 1e9, "positions_per_s": w.B * w.gamma / tm,
-        "mean_accepted": float(acc.float().mean()), "status": int(status.item())}
-    del inp, tokens
+    rows["block_verify_128x7_V129280_bf16"] = bench_block(steps, warmup, flush, stream)
 
     # scheduler, 512 requests x 16 positions
     sw = synth.SCHEDULE
@@ -435,6 +414,55 @@ def bench_schedule(steps, warmup):
     return {"workload": f"{sw.N} requests x {sw.K} positions, B_max={sw.B_max}",
             "us": sum(t) / len(t) * 1e6, "total_rows": int(out["o"]["total_rows"].item()),
             "status": int(status.item())}
+
+
+def bench_block(steps, warmup, flush, stream):
+    """Block verification, 128 requests x 7 drafted positions, V = 129280 bf16."""
+    import torch
+    import speculative_decoding_verification_token_gb300 as sv
+    from speculative_decoding_verification_token_gb300 import synth
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = synth.BLOCK_LARGE
+    inp = synth.token_inputs(w, device=dev)
+    tokens = sv.spec_sample_draft(inp["draft"], inp["draft_row0"], inp["draft_len"], w.gamma,
+                                  w.seed)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = sv.workspace(sv.spec_verify_workspace_bytes(w.B, w.gamma, w.V, sv.SV_BF16), dev)
+    holder = {}
+
+    def blk(want_rows):
+        def call():
+            holder["o"] = sv.spec_verify_block(inp["target"], inp["draft"], inp["target_row0"],
+                                               inp["draft_row0"], inp["draft_len"], w.gamma,
+                                               tokens, w.seed, want_rows=want_rows,
+                                               status=status, workspace=ws)
+        return call
+    # the call a user makes for the tokens alone (no per-row outputs), then the same call with
+    # every running ratio and threshold written (every residual mass computed)
+    t = time_calls(blk(False), steps, warmup, flush, stream)
+    st_tok = int(status.item())
+    acc = holder["o"]["accepted_len"].cpu()
+    t_rows = time_calls(blk(True), steps, warmup, flush, stream)
+    # per-kernel durations of the tokens-only call (block kernel, race kernel)
+    sv.sv_profile_enable(True)
+    parts = []
+    call = blk(False)
+    for _ in range(max(3, steps // 2)):
+        flush()
+        call()
+        parts.append(sv.sv_profile_read())
+    sv.sv_profile_enable(False)
+    kms = [sum(q[k] for q in parts) / len(parts) for k in range(3)]
+    n_bonus = int((acc == w.gamma).sum())
+    nb = (2 * w.B * w.gamma + n_bonus) * w.V * 2
+    tm = sum(t) / len(t)
+    tr = sum(t_rows) / len(t_rows)
+    return {
+        "ms": tm * 1e3, "GB_s": nb / tm / 1e9, "positions_per_s": w.B * w.gamma / tm,
+        "ms_with_row_outputs": tr * 1e3, "GB_s_with_row_outputs": nb / tr / 1e9,
+        "kernel_ms": {"block": round(kms[0], 4), "race": round(kms[2], 4)},
+        "mean_accepted": float(acc.float().mean()),
+        "status": st_tok or int(status.item())}
 
 
 def bench_markov(steps, warmup, flush, stream, positions=None):
@@ -513,6 +541,11 @@ def main():
         row = bench_markov(args.steps, args.warmup, make_flush(torch.device("cuda")),
                            torch.cuda.current_stream(), args.markov_positions)
         print(json.dumps({"row": "markov_draft", **row}))
+        return
+    if args.only == "block":
+        row = bench_block(args.steps, args.warmup, make_flush(torch.device("cuda")),
+                          torch.cuda.current_stream())
+        print(json.dumps({"row": "block_verify", **row}))
         return
     if args.only == "schedule":
         row = bench_schedule(args.steps, args.warmup)

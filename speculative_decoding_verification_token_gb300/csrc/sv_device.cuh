@@ -323,6 +323,7 @@ __device__ __forceinline__ void ms2_vec_f32(float& m, float& s, const uint4& v) 
 // scalar operation would be
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
 // a packed bf16 pair (low half first) widened to binary32, exactly
 __device__ __forceinline__ float2 bf16x2_f2(uint32_t w) {

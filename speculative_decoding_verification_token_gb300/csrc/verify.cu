@@ -1,28 +1,26 @@
 // verify.cu -- token-level and block verification, and draft sampling from q.
 //
-// A verify call is a short chain of kernels on the caller's stream:
+// Token-level verification is two kernels on the caller's stream:
 //   stream  persistent, warp-specialised CTAs (one per SM): a producer warp walks this CTA's
 //           items -- a chunk of one (request, position) row pair -- and feeds a three-deep ring of
 //           32 KB shared-memory stages with bulk copies; sixteen consumer warps fold every staged
-//           element into log2-domain softmax statistics (stats pass) or into the residual mass of
-//           block verification (resid pass); the last warp to finish an item merges the warps'
-//           results into one partial per (row pair, chunk), so no consumer ever waits on another.
-//           Positions are walked highest first, so the early positions -- where the first
-//           rejection and hence the correction race most often fall -- are read last and are
-//           still in L2 when the race reads them again.
-//   decide  one CTA per request: folds the partials of its rows into the row normalisers and
-//           the ratios p(x)/q(x), draws its uniforms, decides the accepted length (token-level)
-//           or the running ratios / thresholds (block), and writes a race descriptor.  For
-//           token-level verification this runs at the start of the race kernel (every CTA of a
-//           request decides, the first writes), so the call is two launches.
-//   race    up to 8 CTAs per request, each staging its contiguous share of the correction (or
-//           bonus) row in shared memory with one bulk copy: exponential race of the share, pruned
-//           against the best seed key any share has published; the shares combine through one
-//           64-bit atomic max per request and the last share to finish writes the outputs.  It is
-//           launched as a programmatic dependent of the stream kernel, so its launch overlaps the
-//           stream's tail.
-// Token-level verification runs stream -> race; block verification runs stream(stats) -> rows
-// -> stream(resid) -> decide -> race.
+//           element into log2-domain softmax statistics; the last warp to finish an item merges
+//           the warps' results into one partial per (row pair, chunk), so no consumer ever waits
+//           on another.  Positions are walked highest first, so the early positions -- where the
+//           first rejection and hence the correction race most often fall -- are read last and
+//           are still in L2 when the race reads them again.
+//   race    up to 8 CTAs per request.  Each first decides its request: it folds the partials of
+//           the request's rows into the row normalisers and the ratios p(x)/q(x), draws the
+//           uniforms and finds the first rejection.  It then stages its contiguous share of the
+//           correction (or bonus) row in shared memory with one bulk copy and runs the exponential
+//           race of the share, pruned against the best seed key any share has published; the
+//           shares combine through one 64-bit atomic max per request and the last share to finish
+//           writes the outputs.  It is launched as a programmatic dependent of the stream kernel,
+//           so its launch overlaps the stream's tail.
+// Block verification is block -> race: the block kernel (one CTA per request, the same producer /
+// consumer ring) walks the request's row pairs in order, each pair's statistics pass from HBM
+// followed by its residual pass re-read from L2, and decides the request; the race kernel then
+// draws its correction or bonus token.
 #include <algorithm>
 #include <mutex>
 
@@ -44,13 +42,6 @@ constexpr size_t kStreamSmem = size_t(kRing) * 2 * kRowBytes;
 constexpr int kRaceSplitMax = 8;                 // CTAs (row shares) per race job
 constexpr uint32_t kRaceShareMax = 64 * 1024;    // largest row share staged in shared memory
 
-struct RowInfo {  // one (request, position) row pair
-  float ratio;    // p(x)/q(x) of the drafted token x
-  float rho;      // block verification: running capped ratio rho_i
-  float h;        // block verification: threshold h_i
-  float pad;
-};
-
 struct RaceDesc {  // per request, written by decide, read by race
   int32_t tau;
   int32_t resid;   // 1: correction from the residual of row pair tau+1; 0: bonus row
@@ -65,11 +56,8 @@ struct RaceSlot {                 // per race job: the shares' combined winner
 };
 
 struct VerifyWs {
-  float4* partials;  // [units * C] (m_t, s_t, m_d, s_d), m in log2 units
-  float4* norms;     // [units] statistics of the whole row pair
-  RowInfo* rows;     // [units]
-  float* rpart;      // [units * C] residual mass per chunk (block)
-  RaceDesc* desc;    // [B]
+  float4* partials;  // [units * C] (m_t, s_t, m_d, s_d), m in log2 units (token-level)
+  RaceDesc* desc;    // [B] (block)
   RaceSlot* slots;   // [units]: verify uses B of them, the sampler one per drafted row
   size_t total;
 };
@@ -99,9 +87,6 @@ static VerifyWs verify_layout(void* base, int32_t B, int32_t gmax, int32_t C) {
   const size_t Bn = size_t(B > 0 ? B : 1);
   const size_t units = Bn * size_t(gmax > 0 ? gmax : 1);
   w.partials = reinterpret_cast<float4*>(take(sizeof(float4) * units * size_t(C)));
-  w.norms = reinterpret_cast<float4*>(take(sizeof(float4) * units));
-  w.rows = reinterpret_cast<RowInfo*>(take(sizeof(RowInfo) * units));
-  w.rpart = reinterpret_cast<float*>(take(sizeof(float) * units * size_t(C)));
   w.desc = reinterpret_cast<RaceDesc*>(take(sizeof(RaceDesc) * Bn));
   w.slots = reinterpret_cast<RaceSlot*>(take(sizeof(RaceSlot) * units));
   w.total = off;
@@ -123,7 +108,6 @@ struct StreamParams {
   const int64_t* draft_row0;
   const int32_t* draft_len;
   int32_t B, gmax, C;
-  int32_t resid_pass;  // 0: softmax statistics; 1: residual masses of positions >= 2
   VerifyWs ws;
   int32_t* status;
 };
@@ -138,17 +122,14 @@ struct StageMeta {
   int64_t e0;     // first vocabulary index of the slice
   const uint8_t* trow;
   const uint8_t* drow;
-  float A, gap, mt, pad;  // residual pass: rho_{i-1} / s_t, gap, m_t (log2 units)
 };
 
 template <typename E>
 __device__ void stream_producer(const StreamParams& p, uint8_t* ring, uint64_t* full,
                                 uint64_t* empty, StageMeta* meta) {
   constexpr int32_t kSE = kRowBytes / esize<E>();
-  const int32_t first_pos = p.resid_pass ? 2 : 1;
-  const int32_t n_pos = p.gmax - first_pos + 1;
   const int64_t per_pos = int64_t(p.B) * p.C;
-  const int64_t n_items = n_pos > 0 ? int64_t(n_pos) * per_pos : 0;
+  const int64_t n_items = int64_t(p.gmax) * per_pos;
   uint32_t n = 0;      // stages issued so far
   int32_t issued = 0;  // items issued so far
   for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -160,17 +141,6 @@ __device__ void stream_producer(const StreamParams& p, uint8_t* ring, uint64_t* 
     const int32_t unit = r * p.gmax + (i - 1);
     const uint8_t* trow = row_ptr<E>(p.target, p.target_row0[r] + (i - 1), p.ld);
     const uint8_t* drow = row_ptr<E>(p.draft, p.draft_row0[r] + (i - 1), p.ld);
-    float A = 0.f, gap = 0.f, mt = 0.f;
-    if (p.resid_pass) {
-      // rho_{i-1} p_i(x) = A 2^(t log2e - m_t), A = rho_{i-1} / s_t, and
-      // q_i(x) / (rho_{i-1} p_i(x)) = exp((d - t) + gap),
-      // gap = (m_t - m_d) ln 2 + log(s_t / (rho_{i-1} s_d))   (+inf when rho_{i-1} = 0)
-      const float4 nm = __ldcg(&p.ws.norms[unit]);
-      const float rho_prev = __ldcg(&p.ws.rows[unit - 1].rho);
-      A = rho_prev / nm.y;
-      gap = (nm.x - nm.z) * kLn2 + (logf(nm.y / nm.w) - logf(rho_prev));
-      mt = nm.x;
-    }
     const int64_t ie0 = int64_t(c) * kSE * kStagesPerItem;
     const int64_t iend = p.V - ie0 < int64_t(kSE) * kStagesPerItem ? p.V
                                                                     : ie0 + int64_t(kSE) * kStagesPerItem;
@@ -188,10 +158,6 @@ __device__ void stream_producer(const StreamParams& p, uint8_t* ring, uint64_t* 
       m.bulk = static_cast<int32_t>(bulk_bytes / esize<E>());
       m.trow = trow;
       m.drow = drow;
-      m.A = A;
-      m.gap = gap;
-      m.mt = mt;
-      m.pad = 0.f;
       meta[stage] = m;
       uint8_t* dst = ring + size_t(stage) * 2 * kRowBytes;
       fence_proxy_async();
@@ -221,7 +187,7 @@ __device__ void stream_consumer(const StreamParams& p, const uint8_t* ring, uint
                                 uint64_t* empty, const StageMeta* meta, MergeSlots* ms) {
   constexpr int kPer = Elem<E>::kPerVec;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float mt = kM2Empty, st = 0.f, md = kM2Empty, sd = 0.f, acc = 0.f;
+  float mt = kM2Empty, st = 0.f, md = kM2Empty, sd = 0.f;
   for (uint32_t n = 0;; ++n) {
     const uint32_t stage = n % kRing;
     if (!mbar_wait(&full[stage], (n / kRing) & 1, p.status)) return;
@@ -230,7 +196,7 @@ __device__ void stream_consumer(const StreamParams& p, const uint8_t* ring, uint
     const uint4* vt = reinterpret_cast<const uint4*>(ring + size_t(stage) * 2 * kRowBytes);
     const uint4* vd = vt + kRowBytes / 16;
     const int nvec = m.bulk / kPer;
-    if (!p.resid_pass && m.bulk == int32_t(kRowBytes / esize<E>())) {
+    if (m.bulk == int32_t(kRowBytes / esize<E>())) {
       // full stage: every consumer thread holds kFull vectors of each row
       constexpr int kFull = int(kRowBytes / 16) / kConsumers;
       static_assert(kFull * kConsumers * 16 == int(kRowBytes), "stage not a whole multiple");
@@ -246,7 +212,7 @@ __device__ void stream_consumer(const StreamParams& p, const uint8_t* ring, uint
         ms2_fold_vecs_f32<kFull>(mt, st, a);
         ms2_fold_vecs_f32<kFull>(md, sd, b);
       }
-    } else if (!p.resid_pass) {
+    } else {
 #pragma unroll 2
       for (int v = tid; v < nvec; v += kConsumers) {
         const uint4 a = vt[v], b = vd[v];
@@ -262,43 +228,20 @@ __device__ void stream_consumer(const StreamParams& p, const uint8_t* ring, uint
         ms2_one(mt, st, Elem<E>::load(m.trow, m.e0 + e));
         ms2_one(md, sd, Elem<E>::load(m.drow, m.e0 + e));
       }
-    } else {
-      // positive part of rho p - q written rho p (1 - exp(y)): accurate relative to itself
-#pragma unroll 2
-      for (int v = tid; v < nvec; v += kConsumers) {
-        float x[kPer], y[kPer];
-        Elem<E>::unpack(vt[v], x);
-        Elem<E>::unpack(vd[v], y);
-#pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-          const float yy = (y[q] - x[q]) + m.gap;
-          if (yy < 0.f) acc += fast_exp2(fmaf(x[q], kLog2e, -m.mt)) * one_minus_exp(yy);
-        }
-      }
-      for (int e = m.bulk + tid; e < m.len; e += kConsumers) {
-        const float x = Elem<E>::load(m.trow, m.e0 + e);
-        const float y = Elem<E>::load(m.drow, m.e0 + e);
-        const float yy = (y - x) + m.gap;
-        if (yy < 0.f) acc += fast_exp2(fmaf(x, kLog2e, -m.mt)) * one_minus_exp(yy);
-      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
     if (!m.last) continue;
     // item complete: each warp leaves its result; the last warp to do so merges and writes
     const int buf = m.item % kRedBufs;
-    if (!p.resid_pass) {
-      warp_ms2(mt, st);
-      warp_ms2(md, sd);
-    } else {
-      acc = warp_sum(acc);
-    }
+    warp_ms2(mt, st);
+    warp_ms2(md, sd);
     int32_t last = 0;
     if (lane == 0) {
       ms->v[buf][warp][0] = mt;
       ms->v[buf][warp][1] = st;
       ms->v[buf][warp][2] = md;
-      ms->v[buf][warp][3] = p.resid_pass ? acc : sd;
+      ms->v[buf][warp][3] = sd;
       __threadfence_block();
       last = atomicAdd(&ms->count[buf], 1) == kConsumerWarps - 1;
     }
@@ -306,29 +249,22 @@ __device__ void stream_consumer(const StreamParams& p, const uint8_t* ring, uint
     if (last) {
       __threadfence_block();
       const size_t slot = size_t(m.unit) * p.C + m.chunk;
-      if (!p.resid_pass) {
-        float a = kM2Empty, b = 0.f, c = kM2Empty, d = 0.f;
-        if (lane < kConsumerWarps) {
-          a = ms->v[buf][lane][0];
-          b = ms->v[buf][lane][1];
-          c = ms->v[buf][lane][2];
-          d = ms->v[buf][lane][3];
-        }
-        warp_ms2(a, b);
-        warp_ms2(c, d);
-        if (lane == 0) __stcg(&p.ws.partials[slot], make_float4(a, b, c, d));
-      } else {
-        float a = lane < kConsumerWarps ? ms->v[buf][lane][3] : 0.f;
-        a = warp_sum(a);
-        if (lane == 0) __stcg(&p.ws.rpart[slot], a * m.A);
+      float a = kM2Empty, b = 0.f, c = kM2Empty, d = 0.f;
+      if (lane < kConsumerWarps) {
+        a = ms->v[buf][lane][0];
+        b = ms->v[buf][lane][1];
+        c = ms->v[buf][lane][2];
+        d = ms->v[buf][lane][3];
       }
+      warp_ms2(a, b);
+      warp_ms2(c, d);
+      if (lane == 0) __stcg(&p.ws.partials[slot], make_float4(a, b, c, d));
       if (lane == 0) ms->count[buf] = 0;
     }
     mt = kM2Empty;
     st = 0.f;
     md = kM2Empty;
     sd = 0.f;
-    acc = 0.f;
   }
 }
 
@@ -360,7 +296,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(StreamParams 
 }
 
 // ---------------------------------------------------------------------------------------------
-// decide: per-request combination of the row statistics and the acceptance decisions
+// decide (token-level): per-request combination of the row statistics and the acceptance test
 // ---------------------------------------------------------------------------------------------
 struct DecideParams {
   const uint8_t* target;
@@ -371,24 +307,41 @@ struct DecideParams {
   const int32_t* draft_len;
   const int32_t* draft_tokens;
   int32_t B, gmax, C;
-  int32_t mode;  // 0: token-level decide; 1: block rows (norms, rho); 2: block decide
   uint64_t seed;
   const uint64_t* request_ids;
-  float* ratio_out;  // token: min(1, p/q); block: rho_i
-  float* h_out;      // block: h_i
+  float* ratio_out;  // min(1, p/q) per drafted row (nullable)
   VerifyWs ws;
   int32_t* status;
 };
 
-// The decision of request r by one CTA.  `writer`: this CTA writes the call's outputs (ratios,
-// row normalisers, the race descriptor in the workspace, the status word); `s_desc` (nullable)
-// receives the race descriptor in shared memory.  Every thread of the CTA must call it.
+// p_j(x)/q_j(x) of the drafted token x from the row pair's statistics nm = (m_t, s_t, m_d, s_d)
+// (log2 domain) and the two logits of x; `bad` flags a data error: an all -inf row (its sum is
+// 0), a NaN or +inf logit (the sum is NaN), x out of range, or q(x) = 0.
+__device__ __forceinline__ float row_ratio(float4 nm, int32_t x, int64_t V, float tx, float dx,
+                                           bool& bad) {
+  bad = !(nm.y > 0.f && nm.y < INFINITY && nm.w > 0.f && nm.w < INFINITY);
+  if (x < 0 || int64_t(x) >= V) {
+    bad = true;
+    return 0.f;
+  }
+  if (!(dx > -INFINITY)) bad = true;  // q(x) = 0: x cannot have been proposed
+  // p(x)/q(x) = 2^((t_x log2e - m_t) - (d_x log2e - m_d)) s_d / s_t
+  return exp2f(fmaf(tx, kLog2e, -nm.x) - fmaf(dx, kLog2e, -nm.z)) * (nm.w / nm.y);
+}
+
+// log of q(x) / (w p(x)) at d = t for the row pair's statistics nm and lnw = log w:
+// (m_t - m_d) ln 2 + log(s_t / s_d) - log w, so that q(x) / (w p(x)) = exp((d - t) + gap).
+__device__ __forceinline__ float resid_gap(float4 nm, float lnw) {
+  return (nm.x - nm.z) * kLn2 + logf(nm.y / nm.w) - lnw;
+}
+
+// The decision of request r by one CTA.  `writer`: this CTA writes the call's ratio outputs and
+// the status word; `s_desc` receives the race descriptor in shared memory.  Every thread of the
+// CTA must call it.
 template <typename E>
 __device__ __noinline__ void decide_body(const DecideParams& p, int32_t r, bool writer,
-                                            RaceDesc* s_desc) {
+                                         RaceDesc* s_desc) {
   __shared__ float s_ratio[SV_MAX_DRAFT_LEN + 1];
-  __shared__ float s_rho[SV_MAX_DRAFT_LEN + 1];
-  __shared__ float s_R[SV_MAX_DRAFT_LEN + 1];
   __shared__ float s_u[SV_MAX_DRAFT_LEN + 1];
   __shared__ float4 s_norm[SV_MAX_DRAFT_LEN + 1];
   __shared__ int32_t s_bad;
@@ -399,122 +352,487 @@ __device__ __noinline__ void decide_body(const DecideParams& p, int32_t r, bool 
   if (tid == 0) s_bad = (graw != g) ? SV_ERR_BAD_INPUT : 0;
   __syncthreads();
 
-  if (p.mode == 0 || p.mode == 1) {
-    // row normalisers and the drafted token's ratio, one warp per row
-    for (int i = warp + 1; i <= g; i += kWarps) {
-      const int32_t unit = r * p.gmax + (i - 1);
-      // lane 0 fetches the drafted token and its two logits while the warp folds the partials
-      const int64_t drow = p.draft_row0[r] + (i - 1);
-      int32_t x = -1;
-      float tx = 0.f, dx = 0.f;
-      if (lane == 0) {
-        x = p.draft_tokens[drow];
-        if (x >= 0 && int64_t(x) < p.V) {
-          tx = Elem<E>::load(row_ptr<E>(p.target, p.target_row0[r] + (i - 1), p.ld), x);
-          dx = Elem<E>::load(row_ptr<E>(p.draft, drow, p.ld), x);
-        }
-      }
-      float mt = kM2Empty, st = 0.f, md = kM2Empty, sd = 0.f;
-      for (int c = lane; c < p.C; c += 32) {
-        const float4 q = __ldcg(&p.ws.partials[size_t(unit) * p.C + c]);
-        ms2_merge(mt, st, q.x, q.y);
-        ms2_merge(md, sd, q.z, q.w);
-      }
-      warp_ms2(mt, st);
-      warp_ms2(md, sd);
-      if (lane == 0) {
-        // an all -inf row sums to 0; NaN or +inf logits make the sum NaN
-        bool bad = !(st > 0.f && st < INFINITY && sd > 0.f && sd < INFINITY);
-        float ratio = 0.f;
-        if (x < 0 || int64_t(x) >= p.V) {
-          bad = true;
-        } else {
-          // p(x)/q(x) = 2^((t_x log2e - m_t) - (d_x log2e - m_d)) s_d / s_t
-          if (!(dx > -INFINITY)) bad = true;  // q(x) = 0: x cannot have been proposed
-          ratio = exp2f(fmaf(tx, kLog2e, -mt) - fmaf(dx, kLog2e, -md)) * (sd / st);
-        }
-        if (bad) s_bad = SV_ERR_BAD_INPUT;
-        s_ratio[i] = ratio;
-        s_norm[i] = make_float4(mt, st, md, sd);
-        if (writer) __stcg(&p.ws.norms[unit], s_norm[i]);
+  // row normalisers and the drafted token's ratio, one warp per row
+  for (int i = warp + 1; i <= g; i += kWarps) {
+    const int32_t unit = r * p.gmax + (i - 1);
+    // lane 0 fetches the drafted token and its two logits while the warp folds the partials
+    const int64_t drow = p.draft_row0[r] + (i - 1);
+    int32_t x = -1;
+    float tx = 0.f, dx = 0.f;
+    if (lane == 0) {
+      x = p.draft_tokens[drow];
+      if (x >= 0 && int64_t(x) < p.V) {
+        tx = Elem<E>::load(row_ptr<E>(p.target, p.target_row0[r] + (i - 1), p.ld), x);
+        dx = Elem<E>::load(row_ptr<E>(p.draft, drow, p.ld), x);
       }
     }
-  } else {
-    // block decide: residual masses R_i (stored at row pair i + 1) and the running ratios
-    for (int i = warp + 1; i < g; i += kWarps) {
-      const int32_t unit = r * p.gmax + i;  // row pair i + 1
-      float a = 0.f;
-      for (int c = lane; c < p.C; c += 32) a += __ldcg(&p.ws.rpart[size_t(unit) * p.C + c]);
-      a = warp_sum(a);
-      if (lane == 0) s_R[i] = a;
+    float mt = kM2Empty, st = 0.f, md = kM2Empty, sd = 0.f;
+    for (int c = lane; c < p.C; c += 32) {
+      const float4 q = __ldcg(&p.ws.partials[size_t(unit) * p.C + c]);
+      ms2_merge(mt, st, q.x, q.y);
+      ms2_merge(md, sd, q.z, q.w);
     }
-    for (int i = tid + 1; i <= g; i += kThreads)
-      s_rho[i] = __ldcg(&p.ws.rows[r * p.gmax + (i - 1)].rho);
+    warp_ms2(mt, st);
+    warp_ms2(md, sd);
+    if (lane == 0) {
+      bool bad = false;
+      const float ratio = row_ratio(make_float4(mt, st, md, sd), x, p.V, tx, dx, bad);
+      if (bad) s_bad = SV_ERR_BAD_INPUT;
+      s_ratio[i] = ratio;
+      s_norm[i] = make_float4(mt, st, md, sd);
+    }
   }
-  // uniforms u_i / eta_i (ACCEPT tag, position i), one thread each
-  if (p.mode != 1)
-    for (int i = tid + 1; i <= g; i += kThreads)
-      s_u[i] = uniform_of(stream_block(make_stream(p.seed, req, i, kTagAccept), 0).x);
+  // uniforms u_i (ACCEPT tag, position i), one thread each
+  for (int i = tid + 1; i <= g; i += kThreads)
+    s_u[i] = uniform_of(stream_block(make_stream(p.seed, req, i, kTagAccept), 0).x);
   __syncthreads();
 
   if (tid == 0) {
     if (writer && s_bad) report(p.status, s_bad);
-    RowInfo* rows = p.ws.rows + size_t(r) * p.gmax;
-    if (p.mode == 1) {
-      // running capped ratios rho_i = min(1, rho_{i-1} p_i(x_i) / q_i(x_i))
-      float rho = 1.f;
-      for (int i = 1; i <= g; ++i) {
-        rho = rho > 0.f ? fminf(1.f, rho * s_ratio[i]) : 0.f;
-        rows[i - 1].rho = rho;
-        if (p.ratio_out) p.ratio_out[p.draft_row0[r] + (i - 1)] = rho;
+    int32_t tau = g;  // walk left to right, stop at the first rejection
+    for (int i = 1; i <= g; ++i)
+      if (!(s_u[i] < s_ratio[i])) {
+        tau = i - 1;
+        break;
       }
-    } else {
-      int32_t tau;
-      float lnw = 0.f;
-      if (p.mode == 0) {
-        tau = g;  // walk left to right, stop at the first rejection
-        for (int i = 1; i <= g; ++i)
-          if (!(s_u[i] < s_ratio[i])) {
-            tau = i - 1;
-            break;
-          }
-      } else {
-        tau = 0;  // longest prefix whose threshold passes
-        for (int i = 1; i <= g; ++i) {
-          float h;
-          if (i < g) {
-            const float den = s_R[i] + (1.f - s_rho[i]);
-            h = den > 0.f ? s_R[i] / den : 1.f;
-          } else {
-            h = s_rho[i];
-          }
-          if (p.h_out) p.h_out[p.draft_row0[r] + (i - 1)] = h;
-          if (s_u[i] <= h) tau = i;
-        }
-        lnw = tau > 0 ? logf(s_rho[tau]) : 0.f;
-      }
-      RaceDesc d;
-      d.tau = tau;
-      d.resid = tau < g;
-      d.gap = 0.f;
-      d.pad = 0;
-      if (d.resid) {
-        // token-level: this CTA's own normalisers; block: those of the rows kernel
-        const float4 nm = p.mode == 0 ? s_norm[tau + 1] : __ldcg(&p.ws.norms[r * p.gmax + tau]);
-        d.gap = (nm.x - nm.z) * kLn2 + logf(nm.y / nm.w) - lnw;
-      }
-      if (writer) p.ws.desc[r] = d;
-      if (s_desc) *s_desc = d;
-    }
+    RaceDesc d;
+    d.tau = tau;
+    d.resid = tau < g;
+    d.gap = d.resid ? resid_gap(s_norm[tau + 1], 0.f) : 0.f;
+    d.pad = 0;
+    *s_desc = d;
   }
-  if (writer && p.mode == 0 && p.ratio_out)
+  if (writer && p.ratio_out)
     for (int i = tid + 1; i <= g; i += kThreads)
       p.ratio_out[p.draft_row0[r] + (i - 1)] = fminf(1.f, s_ratio[i]);
 }
 
+// ---------------------------------------------------------------------------------------------
+// block: one CTA per request -- statistics, running ratios, residual masses and the decision
+// ---------------------------------------------------------------------------------------------
+// Block verification needs, for every i < gamma, the residual mass
+//   R_i = sum_x max(rho_i p_{i+1}(x) - q_{i+1}(x), 0),
+// which depends on the normalisers of row pair i + 1 and on rho_i, i.e. on every earlier pair.
+// The CTA walks its request's row pairs in order: the statistics pass of pair j streams it from
+// HBM, and the residual pass over pair j (with rho_{j-1}) follows at once, re-reading the pair
+// from L2 (about half a megabyte per CTA in flight at V = 129280).
+// The threshold h_i = R_i / (R_i + 1 - rho_i) never exceeds rho_i, because R_i <= rho_i, so a
+// position whose uniform eta_i exceeds rho_i fails whatever R_i is: unless the caller asks for
+// every h_i, the residual pass runs only for positions with eta_i <= rho_i.  The decision is the
+// same either way.
+struct BlockParams {
+  const uint8_t* target;
+  const uint8_t* draft;
+  int64_t V, ld;
+  const int64_t* target_row0;
+  const int64_t* draft_row0;
+  const int32_t* draft_len;
+  const int32_t* draft_tokens;
+  int32_t B, gmax;
+  uint64_t seed;
+  const uint64_t* request_ids;
+  float* rho_out;  // rho_i per drafted row (nullable)
+  float* h_out;    // h_i per drafted row (nullable; non-null computes every R_i)
+  VerifyWs ws;
+  int32_t* status;
+};
+
+enum : int32_t { kSegStats = 0, kSegResid = 1, kSegEnd = 2, kSegExit = 3 };
+
+struct BlockMeta {
+  int32_t kind;  // kSeg*
+  int32_t row;   // row pair j of the request (1-based)
+  int32_t last;  // this stage closes its segment
+  int32_t len;   // elements of the slice
+  int32_t bulk;  // elements brought by the bulk copies (the rest is read from global)
+  int32_t seg;   // running segment number of this CTA (selects the merge buffer)
+  int32_t r;     // request
+  uint32_t seq;  // running request number of this CTA (1, 2, ...)
+  int64_t e0;    // first vocabulary index of the slice
+  const uint8_t* trow;
+  const uint8_t* drow;
+};
+
+constexpr int kBlockRows = SV_MAX_DRAFT_LEN + 1;
+
+struct BlockState {  // the request in flight, in shared memory
+  float4 norm[kBlockRows];       // (m_t, s_t, m_d, s_d) of row pair j, m in log2 units
+  float rho[kBlockRows];         // rho_j
+  float eta[kBlockRows];         // eta_j (ACCEPT uniform of position j)
+  float R[kBlockRows];           // R_i, the residual mass over pair i + 1
+  int32_t cand[kBlockRows];      // R_i is needed: eta_i <= rho_i and i < gamma
+  uint32_t norm_seq[kBlockRows]; // request number whose norm[j] is published
+  uint32_t rho_seq[kBlockRows];  // request number whose rho[j], eta[j], cand[j] are published
+  float dep[kRedBufs][kConsumerWarps][4];
+  int32_t count[kRedBufs];       // warps that have deposited a segment
+  int32_t bad;                   // data error seen in the request in flight
+};
+
+// Wait until the request number in `w` reaches `seq` (bounded; SV_ERR_TIMEOUT on expiry).
+__device__ __forceinline__ bool wait_seq(const uint32_t* w, uint32_t seq, int32_t* status) {
+  const volatile uint32_t* v = w;
+  if (int32_t(*v - seq) >= 0) {
+    __threadfence_block();
+    return true;
+  }
+  const uint64_t t0 = global_ns();
+  while (int32_t(*v - seq) < 0) {
+    if (global_ns() - t0 > 1000000000ull) {
+      report(status, SV_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  __threadfence_block();
+  return true;
+}
+
+__device__ __forceinline__ void publish_seq(uint32_t* w, uint32_t seq) {
+  __threadfence_block();
+  *reinterpret_cast<volatile uint32_t*>(w) = seq;
+}
+
 template <typename E>
-__global__ void __launch_bounds__(kThreads) decide_kernel(DecideParams p) {
-  decide_body<E>(p, blockIdx.x, true, nullptr);
+__device__ void block_producer(const BlockParams& p, uint8_t* ring, uint64_t* full,
+                               uint64_t* empty, BlockMeta* meta, BlockState* bs) {
+  constexpr int32_t kSE = kRowBytes / esize<E>();
+  uint32_t n = 0;   // stages issued so far
+  int32_t seg = 0;  // segments issued so far
+  uint32_t seq = 0;
+  auto acquire = [&](uint32_t& stage) {
+    stage = n % kRing;
+    return n < kRing || mbar_wait(&empty[stage], ((n / kRing) - 1) & 1, p.status);
+  };
+  // every slice of one row pair, as one segment
+  auto issue_pair = [&](int32_t kind, int32_t r, int32_t j) {
+    const uint8_t* trow = row_ptr<E>(p.target, p.target_row0[r] + (j - 1), p.ld);
+    const uint8_t* drow = row_ptr<E>(p.draft, p.draft_row0[r] + (j - 1), p.ld);
+    for (int64_t e0 = 0; e0 < p.V; e0 += kSE) {
+      uint32_t stage;
+      if (!acquire(stage)) return false;
+      BlockMeta m;
+      m.kind = kind;
+      m.row = j;
+      m.last = e0 + kSE >= p.V;
+      m.len = static_cast<int32_t>(p.V - e0 < kSE ? p.V - e0 : kSE);
+      const uint32_t bulk_bytes = (uint32_t(m.len) * esize<E>()) & ~15u;
+      m.bulk = static_cast<int32_t>(bulk_bytes / esize<E>());
+      m.seg = seg;
+      m.r = r;
+      m.seq = seq;
+      m.e0 = e0;
+      m.trow = trow;
+      m.drow = drow;
+      meta[stage] = m;
+      uint8_t* dst = ring + size_t(stage) * 2 * kRowBytes;
+      fence_proxy_async();
+      mbar_expect_tx(&full[stage], 2 * bulk_bytes);
+      if (bulk_bytes) {
+        bulk_g2s(dst, trow + e0 * esize<E>(), bulk_bytes, &full[stage]);
+        bulk_g2s(dst + kRowBytes, drow + e0 * esize<E>(), bulk_bytes, &full[stage]);
+      }
+      ++n;
+    }
+    ++seg;
+    return true;
+  };
+  auto issue_marker = [&](int32_t kind, int32_t r) {
+    uint32_t stage;
+    if (!acquire(stage)) return false;
+    BlockMeta m = {};
+    m.kind = kind;
+    m.last = 1;
+    m.seg = seg;
+    m.r = r;
+    m.seq = seq;
+    meta[stage] = m;
+    mbar_arrive(&full[stage]);
+    ++n;
+    ++seg;
+    return true;
+  };
+  for (int32_t r = blockIdx.x; r < p.B; r += gridDim.x) {
+    ++seq;
+    const int32_t g = clamp_gamma(p.draft_len[r], p.gmax);
+    for (int32_t j = 1; j <= g; ++j) {
+      if (!issue_pair(kSegStats, r, j)) return;
+      if (j >= 2) {
+        // R_{j-1}, over pair j, is needed when eta_{j-1} <= rho_{j-1} or every h is asked for
+        if (!wait_seq(&bs->rho_seq[j - 1], seq, p.status)) return;
+        if ((p.h_out || bs->cand[j - 1]) && !issue_pair(kSegResid, r, j)) return;
+      }
+    }
+    if (!issue_marker(kSegEnd, r)) return;
+  }
+  issue_marker(kSegExit, -1);
+}
+
+// One pair of residual entries: the positive part of rho p - q, written (up to the per-row factor
+// rho / s_t) as 2^(t log2e - m_t) (1 - exp(y)) with y = min((d - t) + gap, 0).  1 - exp(y) is kept
+// accurate relative to itself: near 0 by the Taylor series of -expm1 to degree 6 (truncation below
+// 5e-8 relative for |y| <= 1/4), further out as 1 - 2^(y log2e).  Entries with y >= 0 add 0.
+__device__ __forceinline__ float2 resid_pair(float2 acc, float2 t, float2 d, float2 gap,
+                                             float2 nmt) {
+  float2 y = add2(fma2(t, splat2(-1.f), d), gap);
+  y.x = fminf(y.x, 0.f);
+  y.y = fminf(y.y, 0.f);
+  const float2 e = exp2_2(fma2(t, splat2(kLog2e), nmt));
+  const float2 big = fma2(exp2_2(mul2(y, splat2(kLog2e))), splat2(-1.f), splat2(1.f));
+  float2 s = splat2(-1.f / 720.f);
+  s = fma2(s, y, splat2(-1.f / 120.f));
+  s = fma2(s, y, splat2(-1.f / 24.f));
+  s = fma2(s, y, splat2(-1.f / 6.f));
+  s = fma2(s, y, splat2(-0.5f));
+  s = fma2(s, y, splat2(-1.f));
+  s = mul2(s, y);
+  const float2 om = make_float2(y.x > -0.25f ? s.x : big.x, y.y > -0.25f ? s.y : big.y);
+  return fma2(e, om, acc);
+}
+
+template <typename E>
+__device__ __forceinline__ float2 resid_vec(float2 acc, const uint4& a, const uint4& b,
+                                            float2 gap, float2 nmt) {
+  if constexpr (Elem<E>::kPerVec == 8) {
+    acc = resid_pair(acc, bf16x2_f2(a.x), bf16x2_f2(b.x), gap, nmt);
+    acc = resid_pair(acc, bf16x2_f2(a.y), bf16x2_f2(b.y), gap, nmt);
+    acc = resid_pair(acc, bf16x2_f2(a.z), bf16x2_f2(b.z), gap, nmt);
+    acc = resid_pair(acc, bf16x2_f2(a.w), bf16x2_f2(b.w), gap, nmt);
+  } else {
+    acc = resid_pair(acc, make_float2(__uint_as_float(a.x), __uint_as_float(a.y)),
+                     make_float2(__uint_as_float(b.x), __uint_as_float(b.y)), gap, nmt);
+    acc = resid_pair(acc, make_float2(__uint_as_float(a.z), __uint_as_float(a.w)),
+                     make_float2(__uint_as_float(b.z), __uint_as_float(b.w)), gap, nmt);
+  }
+  return acc;
+}
+
+// The decision of request r, by one warp once every segment of the request is merged: thresholds
+// h_i, the accepted length tau = max{i : eta_i <= h_i} (0 if none), the race descriptor.
+template <typename E>
+__device__ void block_decide(const BlockParams& p, int32_t r, BlockState* bs) {
+  if ((threadIdx.x & 31) != 0) return;
+  const int32_t graw = p.draft_len[r];
+  const int32_t g = clamp_gamma(graw, p.gmax);
+  int32_t tau = 0;
+  for (int32_t i = 1; i <= g; ++i) {
+    float h;
+    if (i == g) {
+      h = bs->rho[i];
+    } else if (p.h_out || bs->cand[i]) {
+      const float den = bs->R[i] + (1.f - bs->rho[i]);
+      h = den > 0.f ? bs->R[i] / den : 1.f;
+    } else {
+      h = -1.f;  // eta_i > rho_i >= h_i: position i fails whatever R_i is
+    }
+    const int64_t row = p.draft_row0[r] + (i - 1);
+    if (p.h_out) p.h_out[row] = h;
+    if (p.rho_out) p.rho_out[row] = bs->rho[i];
+    if (bs->eta[i] <= h) tau = i;
+  }
+  RaceDesc d;
+  d.tau = tau;
+  d.resid = tau < g;
+  d.gap = d.resid ? resid_gap(bs->norm[tau + 1], tau > 0 ? logf(bs->rho[tau]) : 0.f) : 0.f;
+  d.pad = 0;
+  p.ws.desc[r] = d;
+  if (graw != g || bs->bad) report(p.status, SV_ERR_BAD_INPUT);
+  bs->bad = 0;
+}
+
+template <typename E>
+__device__ void block_consumer(const BlockParams& p, const uint8_t* ring, uint64_t* full,
+                               uint64_t* empty, const BlockMeta* meta, BlockState* bs) {
+  constexpr int kPer = Elem<E>::kPerVec;
+  constexpr int kFull = int(kRowBytes / 16) / kConsumers;
+  static_assert(kFull * kConsumers * 16 == int(kRowBytes), "stage not a whole multiple");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float mt = kM2Empty, st = 0.f, md = kM2Empty, sd = 0.f;
+  float2 acc = make_float2(0.f, 0.f);
+  float2 gap = splat2(0.f), nmt = splat2(0.f);
+  float A = 0.f;
+  int32_t cur_seg = -1;
+  for (uint32_t n = 0;; ++n) {
+    const uint32_t stage = n % kRing;
+    if (!mbar_wait(&full[stage], (n / kRing) & 1, p.status)) return;
+    const BlockMeta m = meta[stage];
+    if (m.kind == kSegExit) return;
+    const uint4* vt = reinterpret_cast<const uint4*>(ring + size_t(stage) * 2 * kRowBytes);
+    const uint4* vd = vt + kRowBytes / 16;
+    const int nvec = m.bulk / kPer;
+    const bool whole = m.bulk == int32_t(kRowBytes / esize<E>());
+    if (m.kind == kSegStats) {
+      if (whole) {
+        uint4 a[kFull], b[kFull];
+#pragma unroll
+        for (int u = 0; u < kFull; ++u) a[u] = vt[tid + u * kConsumers];
+#pragma unroll
+        for (int u = 0; u < kFull; ++u) b[u] = vd[tid + u * kConsumers];
+        if constexpr (kPer == 8) {
+          ms2_fold_vecs_bf16<kFull>(mt, st, a);
+          ms2_fold_vecs_bf16<kFull>(md, sd, b);
+        } else {
+          ms2_fold_vecs_f32<kFull>(mt, st, a);
+          ms2_fold_vecs_f32<kFull>(md, sd, b);
+        }
+      } else {
+        for (int v = tid; v < nvec; v += kConsumers) {
+          if constexpr (kPer == 8) {
+            ms2_vec_bf16(mt, st, vt[v]);
+            ms2_vec_bf16(md, sd, vd[v]);
+          } else {
+            ms2_vec_f32(mt, st, vt[v]);
+            ms2_vec_f32(md, sd, vd[v]);
+          }
+        }
+        for (int e = m.bulk + tid; e < m.len; e += kConsumers) {
+          ms2_one(mt, st, Elem<E>::load(m.trow, m.e0 + e));
+          ms2_one(md, sd, Elem<E>::load(m.drow, m.e0 + e));
+        }
+      }
+    } else if (m.kind == kSegResid) {
+      if (m.seg != cur_seg) {
+        // first stage of the residual pass over pair j: rho_{j-1} p_j(x) = A 2^(t log2e - m_t)
+        // with A = rho_{j-1} / s_t, and q_j(x) / (rho_{j-1} p_j(x)) = exp((d - t) + gap)
+        int32_t ok = 1;
+        if (lane == 0)
+          ok = wait_seq(&bs->norm_seq[m.row], m.seq, p.status) &&
+               wait_seq(&bs->rho_seq[m.row - 1], m.seq, p.status);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+        __syncwarp();
+        const float4 nm = bs->norm[m.row];
+        const float rho_prev = bs->rho[m.row - 1];
+        A = rho_prev / nm.y;
+        gap = splat2(resid_gap(nm, logf(rho_prev)));
+        nmt = splat2(-nm.x);
+        cur_seg = m.seg;
+      }
+      if (whole) {
+        uint4 a[kFull], b[kFull];
+#pragma unroll
+        for (int u = 0; u < kFull; ++u) a[u] = vt[tid + u * kConsumers];
+#pragma unroll
+        for (int u = 0; u < kFull; ++u) b[u] = vd[tid + u * kConsumers];
+#pragma unroll
+        for (int u = 0; u < kFull; ++u) acc = resid_vec<E>(acc, a[u], b[u], gap, nmt);
+      } else {
+        for (int v = tid; v < nvec; v += kConsumers) acc = resid_vec<E>(acc, vt[v], vd[v], gap, nmt);
+        for (int e = m.bulk + tid; e < m.len; e += kConsumers) {
+          const float2 t = make_float2(Elem<E>::load(m.trow, m.e0 + e), -INFINITY);
+          const float2 d = make_float2(Elem<E>::load(m.drow, m.e0 + e), -INFINITY);
+          acc = resid_pair(acc, t, d, gap, nmt);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (!m.last) continue;
+
+    // segment complete: each warp leaves its result; the last warp to do so merges
+    const int buf = m.seg % kRedBufs;
+    if (m.kind == kSegStats) {
+      warp_ms2(mt, st);
+      warp_ms2(md, sd);
+    } else if (m.kind == kSegResid) {
+      st = warp_sum(acc.x + acc.y);
+    }
+    int32_t last = 0;
+    if (lane == 0) {
+      bs->dep[buf][warp][0] = mt;
+      bs->dep[buf][warp][1] = st;
+      bs->dep[buf][warp][2] = md;
+      bs->dep[buf][warp][3] = sd;
+      __threadfence_block();
+      last = atomicAdd(&bs->count[buf], 1) == kConsumerWarps - 1;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __threadfence_block();
+      if (m.kind == kSegStats) {
+        float a = kM2Empty, b = 0.f, c = kM2Empty, d = 0.f;
+        if (lane < kConsumerWarps) {
+          a = bs->dep[buf][lane][0];
+          b = bs->dep[buf][lane][1];
+          c = bs->dep[buf][lane][2];
+          d = bs->dep[buf][lane][3];
+        }
+        warp_ms2(a, b);
+        warp_ms2(c, d);
+        if (lane == 0) {
+          const int32_t j = m.row;
+          const float4 nm = make_float4(a, b, c, d);
+          bs->norm[j] = nm;
+          publish_seq(&bs->norm_seq[j], m.seq);  // the residual pass over pair j may start
+          // ratio p_j(x_j) / q_j(x_j) and the running ratio rho_j = min(1, rho_{j-1} ratio)
+          const int64_t drow = p.draft_row0[m.r] + (j - 1);
+          const int32_t x = p.draft_tokens[drow];
+          float tx = 0.f, dx = 0.f;
+          if (x >= 0 && int64_t(x) < p.V) {
+            tx = Elem<E>::load(m.trow, x);
+            dx = Elem<E>::load(m.drow, x);
+          }
+          bool bad = false;
+          const float ratio = row_ratio(nm, x, p.V, tx, dx, bad);
+          if (bad) bs->bad = 1;
+          float rho_prev = 1.f;  // on an expired wait the status word already says so
+          if (j > 1) rho_prev = wait_seq(&bs->rho_seq[j - 1], m.seq, p.status) ? bs->rho[j - 1] : 0.f;
+          const float rho = rho_prev > 0.f ? fminf(1.f, rho_prev * ratio) : 0.f;
+          const uint64_t req = p.request_ids ? p.request_ids[m.r] : uint64_t(m.r);
+          const float eta =
+              uniform_of(stream_block(make_stream(p.seed, req, j, kTagAccept), 0).x);
+          const int32_t g = clamp_gamma(p.draft_len[m.r], p.gmax);
+          bs->rho[j] = rho;
+          bs->eta[j] = eta;
+          bs->cand[j] = j < g && eta <= rho;
+          publish_seq(&bs->rho_seq[j], m.seq);
+        }
+      } else if (m.kind == kSegResid) {
+        float a = lane < kConsumerWarps ? bs->dep[buf][lane][1] : 0.f;
+        a = warp_sum(a);
+        if (lane == 0) bs->R[m.row - 1] = a * A;
+      } else {
+        block_decide<E>(p, m.r, bs);
+      }
+      __syncwarp();
+      if (lane == 0) bs->count[buf] = 0;
+    }
+    mt = kM2Empty;
+    st = 0.f;
+    md = kM2Empty;
+    sd = 0.f;
+    acc = make_float2(0.f, 0.f);
+  }
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kStreamThreads, 1) block_kernel(BlockParams p) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t full[kRing], empty[kRing];
+  __shared__ BlockMeta meta[kRing];
+  __shared__ BlockState bs;
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kRing; ++k) {
+      mbar_init(&full[k], 1);
+      mbar_init(&empty[k], kConsumerWarps);
+    }
+    for (int k = 0; k < kRedBufs; ++k) bs.count[k] = 0;
+    for (int k = 0; k < kBlockRows; ++k) {
+      bs.norm_seq[k] = 0u;
+      bs.rho_seq[k] = 0u;
+    }
+    bs.bad = 0;
+    fence_barrier_init();
+  }
+  // the race kernel that follows may launch now (it waits for this grid's results itself)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == 0)  // the race's per-request slots start empty
+    for (int i = threadIdx.x; i < p.B; i += blockDim.x) p.ws.slots[i] = RaceSlot{0ull, 0u, 0u};
+  __syncthreads();
+  if (warp == kConsumerWarps) {
+    if ((threadIdx.x & 31) == 0) block_producer<E>(p, ring, full, empty, meta, &bs);
+  } else {
+    block_consumer<E>(p, ring, full, empty, meta, &bs);
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -724,13 +1042,26 @@ static sv_status launch_stream(const StreamParams& sp, cudaStream_t stream) {
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kStreamSmem)) !=
       cudaSuccess)
     return SV_ERR_CUDA;
-  const int first_pos = sp.resid_pass ? 2 : 1;
-  const int64_t items = int64_t(std::max(0, sp.gmax - first_pos + 1)) * sp.B * sp.C;
+  const int64_t items = int64_t(sp.gmax) * sp.B * sp.C;
   if (items == 0) return SV_OK;
   const int sms = device_sm_count();
   if (sms <= 0) return SV_ERR_CUDA;
   const unsigned grid = unsigned(std::min<int64_t>(items, sms));
   stream_kernel<E><<<grid, kStreamThreads, kStreamSmem, stream>>>(sp);
+  return SV_OK;
+}
+
+// One CTA per request while the requests fit on the SMs (one CTA per SM), else a persistent grid.
+template <typename E>
+static sv_status launch_block(const BlockParams& bp, cudaStream_t stream) {
+  const void* kfn = reinterpret_cast<const void*>(&block_kernel<E>);
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kStreamSmem)) !=
+      cudaSuccess)
+    return SV_ERR_CUDA;
+  const int sms = device_sm_count();
+  if (sms <= 0) return SV_ERR_CUDA;
+  const unsigned grid = unsigned(std::min<int64_t>(bp.B, sms));
+  block_kernel<E><<<grid, kStreamThreads, kStreamSmem, stream>>>(bp);
   return SV_OK;
 }
 
@@ -773,63 +1104,75 @@ static sv_status run_verify(bool block, const CommonArgs& a, const int64_t* targ
   if (status && cudaMemsetAsync(status, 0, sizeof(int32_t), stream) != cudaSuccess)
     return SV_ERR_CUDA;
 
-  StreamParams sp;
-  sp.target = static_cast<const uint8_t*>(a.target);
-  sp.draft = static_cast<const uint8_t*>(a.draft);
-  sp.V = a.V;
-  sp.ld = a.ld;
-  sp.target_row0 = target_row0;
-  sp.draft_row0 = draft_row0;
-  sp.draft_len = draft_len;
-  sp.B = a.B;
-  sp.gmax = a.gmax;
-  sp.C = C;
-  sp.resid_pass = 0;
-  sp.ws = ws;
-  sp.status = status;
-  profile_mark(0, stream);
-  sv_status st = launch_stream<E>(sp, stream);
-  if (st != SV_OK) return st;
-  if (a.gmax == 0 &&  // no stream launch: the race slots are zeroed here instead
-      cudaMemsetAsync(ws.slots, 0, sizeof(RaceSlot) * size_t(a.B), stream) != cudaSuccess)
-    return SV_ERR_CUDA;
-
-  DecideParams dp;
-  dp.target = sp.target;
-  dp.draft = sp.draft;
-  dp.V = a.V;
-  dp.ld = a.ld;
-  dp.target_row0 = target_row0;
-  dp.draft_row0 = draft_row0;
-  dp.draft_len = draft_len;
-  dp.draft_tokens = draft_tokens;
-  dp.B = a.B;
-  dp.gmax = a.gmax;
-  dp.C = C;
-  dp.seed = seed;
-  dp.request_ids = request_ids;
-  dp.ratio_out = ratio_out;
-  dp.h_out = h_out;
-  dp.ws = ws;
-  dp.status = status;
+  const uint8_t* target = static_cast<const uint8_t*>(a.target);
+  const uint8_t* draft = static_cast<const uint8_t*>(a.draft);
+  DecideParams dp = {};
+  sv_status st;
   if (!block) {
-    profile_mark(1, stream);  // token-level: the race kernel decides (no kernel in between)
-    dp.mode = 0;
-  } else {
-    dp.mode = 1;
-    decide_kernel<E><<<a.B, kThreads, 0, stream>>>(dp);
-    sp.resid_pass = 1;
+    StreamParams sp;
+    sp.target = target;
+    sp.draft = draft;
+    sp.V = a.V;
+    sp.ld = a.ld;
+    sp.target_row0 = target_row0;
+    sp.draft_row0 = draft_row0;
+    sp.draft_len = draft_len;
+    sp.B = a.B;
+    sp.gmax = a.gmax;
+    sp.C = C;
+    sp.ws = ws;
+    sp.status = status;
+    profile_mark(0, stream);
     st = launch_stream<E>(sp, stream);
     if (st != SV_OK) return st;
+    if (a.gmax == 0 &&  // no stream launch: the race slots are zeroed here instead
+        cudaMemsetAsync(ws.slots, 0, sizeof(RaceSlot) * size_t(a.B), stream) != cudaSuccess)
+      return SV_ERR_CUDA;
+    profile_mark(1, stream);  // the race kernel decides (no kernel in between)
+    dp.target = target;
+    dp.draft = draft;
+    dp.V = a.V;
+    dp.ld = a.ld;
+    dp.target_row0 = target_row0;
+    dp.draft_row0 = draft_row0;
+    dp.draft_len = draft_len;
+    dp.draft_tokens = draft_tokens;
+    dp.B = a.B;
+    dp.gmax = a.gmax;
+    dp.C = C;
+    dp.seed = seed;
+    dp.request_ids = request_ids;
+    dp.ratio_out = ratio_out;
+    dp.ws = ws;
+    dp.status = status;
+  } else {
+    BlockParams bp;
+    bp.target = target;
+    bp.draft = draft;
+    bp.V = a.V;
+    bp.ld = a.ld;
+    bp.target_row0 = target_row0;
+    bp.draft_row0 = draft_row0;
+    bp.draft_len = draft_len;
+    bp.draft_tokens = draft_tokens;
+    bp.B = a.B;
+    bp.gmax = a.gmax;
+    bp.seed = seed;
+    bp.request_ids = request_ids;
+    bp.rho_out = ratio_out;
+    bp.h_out = h_out;
+    bp.ws = ws;
+    bp.status = status;
+    profile_mark(0, stream);
+    st = launch_block<E>(bp, stream);
+    if (st != SV_OK) return st;
     profile_mark(1, stream);
-    dp.mode = 2;
-    decide_kernel<E><<<a.B, kThreads, 0, stream>>>(dp);
   }
   profile_mark(2, stream);
 
   RaceParams rp = {};
-  rp.target = sp.target;
-  rp.draft = sp.draft;
+  rp.target = target;
+  rp.draft = draft;
   rp.V = a.V;
   rp.ld = a.ld;
   rp.target_row0 = target_row0;
@@ -1022,7 +1365,8 @@ extern "C" sv_status spec_verify_token_noalloc(
   const sv_status st = sv::noalloc_scratch_address(&scratch);
   if (st != SV_OK) return st;
   // The verify kernels never read scratch they have not written earlier in the same call; the
-  // only counters (race tickets) are cleared by the decide kernel before the race kernel runs.
+  // only counters (race tickets) are cleared by the call's first kernel before the race kernel
+  // runs.
   return spec_verify_token(target_logits, draft_logits, dtype, V, ld, target_row0, draft_row0,
                            draft_len, max_draft_len, draft_tokens, B, seed, request_ids,
                            accepted_len, out_tokens, out_ld, correction_token, accept_ratio,

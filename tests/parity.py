@@ -62,6 +62,9 @@ def compare_verify(gpu, ref, block, lens, draft_row0, report=None):
     # per-position probabilities of every drafted row
     rows = np.concatenate([np.arange(r0, r0 + g) for r0, g in zip(draft_row0, lens)]).astype(
         np.int64) if len(lens) else np.zeros(0, np.int64)
+    row_out = gpu.get("running_ratio" if block else "accept_ratio")
+    if row_out is None:  # the call left out its per-row outputs
+        rows = rows[:0]
     if rows.size:
         if block:
             g_rho = gpu["running_ratio"].cpu().numpy()[rows]

@@ -29,26 +29,34 @@ def _to_dev(inp):
     return d
 
 
-def _run(sv, block, inp, tokens, request_ids=None):
-    fn = sv.spec_verify_block if block else sv.spec_verify_token
-    out = fn(inp["target"], inp["draft"], inp["target_row0"], inp["draft_row0"],
-             inp["draft_len"], inp["max_draft_len"], torch.from_numpy(tokens).cuda(),
-             inp["seed"], request_ids=request_ids)
+def _run(sv, block, inp, tokens, request_ids=None, want_rows=True):
+    """want_rows=False leaves out the per-row outputs; block verification then computes the
+    residual mass only for positions whose uniform does not exceed the running ratio."""
+    if block:
+        out = sv.spec_verify_block(inp["target"], inp["draft"], inp["target_row0"],
+                                   inp["draft_row0"], inp["draft_len"], inp["max_draft_len"],
+                                   torch.from_numpy(tokens).cuda(), inp["seed"],
+                                   request_ids=request_ids, want_rows=want_rows)
+    else:
+        out = sv.spec_verify_token(inp["target"], inp["draft"], inp["target_row0"],
+                                   inp["draft_row0"], inp["draft_len"], inp["max_draft_len"],
+                                   torch.from_numpy(tokens).cuda(), inp["seed"],
+                                   request_ids=request_ids, want_ratio=want_rows)
     torch.cuda.synchronize()
     assert int(out["status"].item()) == 0, sv.status_string(int(out["status"].item()))
     return out
 
 
-def _parity(sv, orc, block, inp, tokens=None, request_ids=None):
+def _parity(sv, orc, block, inp, tokens=None, request_ids=None, want_rows=True):
     if tokens is None:
         tokens = oracle_tokens(orc, inp)
     rid_np = None if request_ids is None else request_ids.cpu().numpy()
     ref = oracle_verify(orc, block, inp, tokens, request_ids=rid_np)
     assert ref["status"] == 0
-    gpu = _run(sv, block, inp, tokens, request_ids)
+    gpu = _run(sv, block, inp, tokens, request_ids, want_rows=want_rows)
     lay = layout_np(inp)
     res = compare_verify(gpu, ref, block, lay["draft_len"], lay["draft_row0"])
-    print(f"\n[parity] block={block} B={inp['B']} V={inp['V']}: {res}")
+    print(f"\n[parity] block={block} rows={want_rows} B={inp['B']} V={inp['V']}: {res}")
     return gpu, ref, res
 
 
@@ -65,7 +73,12 @@ def test_scaled_bf16_ragged_vocab(sv, orc, block, V):
     """bf16 rows spanning several 16 KB slices with a ragged tail (V not a multiple of 8 uses a
     padded row stride)."""
     w = synth.scaled(synth.TOKEN_LARGE, B=12, V=V)
-    inp = synth.token_inputs(w, device="cpu")
+    _parity(sv, orc, block, _padded_dev(synth.token_inputs(w, device="cpu")))
+
+
+def _padded_dev(inp):
+    """Device copy whose rows are padded to a 16-byte stride (V not a multiple of 8)."""
+    V = inp["V"]
     ld = (V + 7) // 8 * 8
     for k in ("target", "draft"):
         buf = torch.zeros((inp[k].shape[0], ld), dtype=inp[k].dtype)
@@ -74,7 +87,7 @@ def test_scaled_bf16_ragged_vocab(sv, orc, block, V):
     inp = _to_dev(inp)
     inp["target"] = inp["target"][:, :V]
     inp["draft"] = inp["draft"][:, :V]
-    _parity(sv, orc, block, inp)
+    return inp
 
 
 @pytest.mark.parametrize("block", [0, 1])
@@ -99,6 +112,32 @@ def test_full_size_workloads(sv, orc, block):
     w = synth.BLOCK_LARGE if block else synth.TOKEN_LARGE
     inp = _to_dev(synth.token_inputs(w, device="cpu"))
     _parity(sv, orc, block, inp)
+
+
+@pytest.mark.parametrize("case", ["small_f32", "ragged_vocab", "ragged_lengths", "full_size"])
+def test_block_without_row_outputs(sv, orc, case):
+    """Block verification without the per-row outputs skips the residual pass of positions whose
+    uniform exceeds the running ratio (h_i <= rho_i < eta_i fails whatever R_i is).  Accepted
+    lengths and tokens must still equal the oracle's; and, on the same inputs, the call with the
+    per-row outputs must agree with it exactly."""
+    rids = None
+    if case == "small_f32":
+        inp = _to_dev(synth.token_inputs(synth.TOKEN_SMALL, device="cpu"))
+    elif case == "ragged_vocab":
+        inp = _padded_dev(synth.token_inputs(synth.scaled(synth.BLOCK_LARGE, B=24, V=40003),
+                                             device="cpu"))
+    elif case == "ragged_lengths":
+        w = synth.scaled(synth.BLOCK_LARGE, B=40, V=20000)
+        inp = synth.token_inputs(w, device="cpu", draft_len=synth.ragged_lengths(40, 7, seed=9))
+        inp = _to_dev(inp)
+        rids = torch.arange(1000, 1040, dtype=torch.int64).cuda()
+    else:
+        inp = _to_dev(synth.token_inputs(synth.BLOCK_LARGE, device="cpu"))
+    tokens = oracle_tokens(orc, inp)
+    gpu, _, _ = _parity(sv, orc, 1, inp, tokens=tokens, request_ids=rids, want_rows=False)
+    full = _run(sv, 1, inp, tokens, request_ids=rids, want_rows=True)
+    assert torch.equal(gpu["accepted_len"], full["accepted_len"])
+    assert torch.equal(gpu["out_tokens"], full["out_tokens"])
 
 
 def test_sampler_matches_oracle(sv, orc):
@@ -127,17 +166,20 @@ def test_determinism(sv, orc):
     assert torch.equal(a["accept_ratio"], b["accept_ratio"])
 
 
-def test_all_zero_drafts_and_masked_rows(sv, orc):
+@pytest.mark.parametrize("block", [0, 1])
+def test_all_zero_drafts_and_masked_rows(sv, orc, block):
     """gamma = 0 everywhere (bonus only) and rows with masked (-inf) entries."""
     w = synth.scaled(synth.TOKEN_LARGE, B=6, V=9000)
     inp = synth.token_inputs(w, "cpu", draft_len=np.zeros(6, np.int32))
     inp["target"][:, :4000] = float("-inf")
     inp = _to_dev(inp)
-    gpu, ref, _ = _parity(sv, orc, 0, inp, tokens=np.zeros(inp["draft"].shape[0], np.int32))
+    gpu, ref, _ = _parity(sv, orc, block, inp,
+                          tokens=np.zeros(inp["draft"].shape[0], np.int32))
     assert (gpu["correction"].cpu().numpy() >= 4000).all()
 
 
-def test_data_errors_reported(sv, orc):
+@pytest.mark.parametrize("block", [0, 1])
+def test_data_errors_reported(sv, orc, block):
     w = synth.scaled(synth.TOKEN_SMALL, B=2)
     base = synth.token_inputs(w, "cpu")
     tokens = oracle_tokens(orc, base)
@@ -155,9 +197,9 @@ def test_data_errors_reported(sv, orc):
     cases.append((bad_len, tokens))
     for inp, toks in cases:
         d = _to_dev(inp)
-        out = sv.spec_verify_token(d["target"], d["draft"], d["target_row0"], d["draft_row0"],
-                                   d["draft_len"], d["max_draft_len"],
-                                   torch.from_numpy(toks).cuda(), d["seed"])
+        fn = sv.spec_verify_block if block else sv.spec_verify_token
+        out = fn(d["target"], d["draft"], d["target_row0"], d["draft_row0"], d["draft_len"],
+                 d["max_draft_len"], torch.from_numpy(toks).cuda(), d["seed"])
         torch.cuda.synchronize()
         assert int(out["status"].item()) == sv.SV_ERR_BAD_INPUT
 

@@ -354,12 +354,15 @@ def bench_rows(steps, warmup):
     c = torch.from_numpy(si["cond_accept"]).to(dev)
     ml = torch.from_numpy(si["max_len"]).to(dev)
     sps = torch.from_numpy(si["sps"]).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sws = sv.workspace(sv.dspark_schedule_workspace_bytes(sw.N, sw.K), dev)
     sched = {}
 
     def sch():
-        sched["o"] = sv.dspark_schedule(c, ml, sps, si["B_max"], status=status)
+        sched["o"] = sv.dspark_schedule(c, ml, sps, si["B_max"], status=status, workspace=sws)
     t = time_calls(sch, steps, warmup, flush, stream)  # the flush keeps the GPU ahead of the host
     rows["schedule_512x16"] = {"us": sum(t) / len(t) * 1e6,
+                               "kernel_us": schedule_kernel_us(sch, steps, flush),
                                "total_rows": int(sched["o"]["total_rows"].item()),
                                "status": int(status.item())}
 
@@ -372,7 +375,7 @@ def bench_rows(steps, warmup):
     rnd = {}
 
     def round_():
-        s = sv.dspark_schedule(c, ml, sps, si["B_max"], status=status)
+        s = sv.dspark_schedule(c, ml, sps, si["B_max"], status=status, workspace=sws)
         rnd["o"] = sv.spec_verify_token(vin["target"], vin["draft"], vin["target_row0"],
                                         vin["draft_row0"], s["sel_len"], vw.gamma, vt, vw.seed,
                                         status=status, workspace=ws2)
@@ -406,14 +409,30 @@ def bench_schedule(steps, warmup):
     ml = torch.from_numpy(si["max_len"]).to(dev)
     sps = torch.from_numpy(si["sps"]).to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = sv.workspace(sv.dspark_schedule_workspace_bytes(sw.N, sw.K), dev)
     out = {}
 
     def sch():
-        out["o"] = sv.dspark_schedule(c, ml, sps, si["B_max"], status=status)
+        out["o"] = sv.dspark_schedule(c, ml, sps, si["B_max"], status=status, workspace=ws)
     t = time_calls(sch, steps, warmup, flush, torch.cuda.current_stream())
     return {"workload": f"{sw.N} requests x {sw.K} positions, B_max={sw.B_max}",
-            "us": sum(t) / len(t) * 1e6, "total_rows": int(out["o"]["total_rows"].item()),
-            "status": int(status.item())}
+            "us": sum(t) / len(t) * 1e6, "kernel_us": schedule_kernel_us(sch, steps, flush),
+            "total_rows": int(out["o"]["total_rows"].item()), "status": int(status.item())}
+
+
+def schedule_kernel_us(call, steps, flush):
+    """Device durations of the scheduler's two kernels (rank, admit), from the CUDA events the
+    library records around them when profiling is on."""
+    import speculative_decoding_verification_token_gb300 as sv
+    sv.sv_profile_enable(True)
+    parts = []
+    for _ in range(max(3, steps // 2)):
+        flush()
+        call()
+        parts.append(sv.sv_profile_read())
+    sv.sv_profile_enable(False)
+    return {"rank": round(sum(q[0] for q in parts) / len(parts) * 1e3, 2),
+            "admit": round(sum(q[2] for q in parts) / len(parts) * 1e3, 2)}
 
 
 def bench_block(steps, warmup, flush, stream):

@@ -9,6 +9,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int g_sm_count[kMaxDevices] = {0};
+int g_smem_per_sm[kMaxDevices] = {0};
 }  // namespace
 
 int device_sm_count() {
@@ -21,6 +22,20 @@ int device_sm_count() {
     g_sm_count[dev] = n;
   }
   return g_sm_count[dev];
+}
+
+int device_smem_per_sm() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_smem_per_sm[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+        cudaSuccess)
+      return 0;
+    g_smem_per_sm[dev] = n;
+  }
+  return g_smem_per_sm[dev];
 }
 
 int resident_ctas(const void* kernel, int threads, size_t smem) {

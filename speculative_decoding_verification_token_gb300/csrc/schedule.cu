@@ -1,21 +1,23 @@
-// schedule.cu -- DSpark's hardware-aware prefix scheduler in one CTA.
+// schedule.cu -- DSpark's hardware-aware prefix scheduler: two kernels on the caller's stream.
 //
-//   1. the conditional acceptance probabilities are staged in shared memory (coalesced); survival
-//      products S[i][k] = c[i][1] * ... * c[i][k] (sequential binary32, one thread per request)
-//      and one 64-bit key per extendable prefix (i, k):
-//        key = (~bits(S) << 32) | (k << 20) | i
-//      ascending keys order prefixes by S descending, then k ascending, then i ascending (S >= 0,
-//      whose bit patterns are monotone in the value); unused slots get the all-ones key;
-//   2. bitonic sort of the keys, each thread holding a contiguous run of KPT keys in registers:
-//      strides below KPT swap within a thread, strides below 32 KPT exchange through warp
-//      shuffles, only the longer ones go through shared memory;
-//   3. F = floor(S * 2^40) in sorted order (every thread sums its own run) and an exclusive int64
-//      scan of the runs: T(b) = N * 2^40 + (sum of the first b values of F), exact and independent
-//      of the summation order;
-//   4. f(b) = (double) T(b) * 2^-40 * sps[N + b]; the admitted count b* is the first b with
-//      f(b + 1) <= f(b) (early stop; a min-reduction over b), capped by the item count and by B_max;
-//   5. sel_len[i] = admitted prefixes of request i (prefix-closed by the ordering), counted with
-//      shared-memory atomics and written once.
+//   rank   (every SM; one warp per extendable prefix)  each CTA stages the conditional acceptance
+//          probabilities in shared memory (coalesced), forms the survival products
+//          S[i][k] = c[i][1] * ... * c[i][k] (sequential binary32, one thread per request) and one
+//          64-bit key per extendable prefix (i, k):
+//            key = (~bits(S) << 32) | (k << 20) | i
+//          ascending keys order prefixes by S descending, then k ascending, then i ascending (S >= 0,
+//          whose bit patterns are monotone in the value).  S never grows with k, so each request's
+//          keys form an ascending run, and the rank of a prefix in the global order is the sum over
+//          the runs of the number of their keys below its own -- one binary search per run, the
+//          lanes of a warp splitting the runs.  The rank places F = floor(S * 2^40) in sorted order
+//          and is kept per prefix.
+//   admit  (one CTA, a programmatic dependent of rank)  an exclusive int64 scan of F in sorted
+//          order gives T(b) = N * 2^40 + (sum of the first b values of F), exact and independent of
+//          the summation order; f(b) = (double) T(b) * 2^-40 * sps[N + b]; the admitted count b* is
+//          the first b with f(b + 1) <= f(b) (early stop; a min-reduction over b), capped by the
+//          item count and by B_max; sel_len[i] counts the prefixes of request i ranked below b*
+//          (prefix-closed by the ordering).
+#include <algorithm>
 #include <cstdint>
 
 #include "sv_device.cuh"
@@ -23,6 +25,9 @@
 
 namespace sv {
 
+constexpr int kChunkThreads = 512;
+constexpr int kChunkSlots = 512;  // keys per chunk (at least one request's K)
+constexpr int kRankThreads = 512;
 constexpr int kSchedThreads = 1024;
 constexpr int kSchedWarps = kSchedThreads / 32;
 constexpr int kSchedMaxItems = 16384;
@@ -35,144 +40,247 @@ struct ScheduleParams {
   int32_t N, K;
   const double* sps;
   int32_t B_max;
-  int32_t n_pad;  // 1024 * KPT >= N * K
   int32_t* sel_len;
   float* survival;
   int32_t* total_rows;
   double* objective;
   int32_t* status;
+  int32_t R;              // requests per chunk
+  int32_t CL;             // keys per chunk (R * K)
+  int32_t n_chunks;       // ceil(N / R)
+  uint64_t* chunk_keys;   // workspace [n_chunks][CL]: each chunk's keys, sorted
+  long long* sorted_F;    // workspace [N * K]: F of the prefix of rank b, at b
+  int32_t* sorted_req;    // workspace [N * K]: the request of the prefix of rank b, at b
 };
+
+static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 __device__ __forceinline__ long long fixed40(uint64_t key) {
   const float S = __uint_as_float(~static_cast<uint32_t>(key >> 32));
   return static_cast<long long>(floor(static_cast<double>(S) * kTwo40));
 }
 
-// Ascending bitonic sort of the n = kSchedThreads * KPT keys held as v[j] = element tid * KPT + j.
-template <int KPT>
-__device__ __forceinline__ void bitonic_sort(uint64_t (&v)[KPT], uint64_t* sm, int tid) {
-  constexpr int n = kSchedThreads * KPT;
-  for (int size = 2; size <= n; size <<= 1) {
-    int stride = size >> 1;
-    if (stride >= 32 * KPT) {
-      // partners in other warps: through shared memory
-#pragma unroll
-      for (int j = 0; j < KPT; ++j) sm[tid * KPT + j] = v[j];
-      __syncthreads();
-      for (; stride >= 32 * KPT; stride >>= 1) {
-        for (int t = tid; t < n / 2; t += kSchedThreads) {
-          const int lo = 2 * t - (t & (stride - 1));
-          const int hi = lo + stride;
-          const bool up = (lo & size) == 0;
-          const uint64_t a = sm[lo], b = sm[hi];
-          if ((a > b) == up) {
-            sm[lo] = b;
-            sm[hi] = a;
-          }
-        }
-        __syncthreads();
-      }
-#pragma unroll
-      for (int j = 0; j < KPT; ++j) v[j] = sm[tid * KPT + j];
-    }
-    // partners in other lanes of this warp: element tid * KPT + j pairs with lane tid ^ (stride /
-    // KPT), same j
-    for (; stride >= KPT; stride >>= 1) {
-      const int ts = stride / KPT;
-#pragma unroll
-      for (int j = 0; j < KPT; ++j) {
-        const uint64_t o = __shfl_xor_sync(0xffffffffu, v[j], ts);
-        const int g = tid * KPT + j;
-        const bool up = (g & size) == 0;
-        const bool lower = (g & stride) == 0;
-        v[j] = (lower == up) ? (v[j] < o ? v[j] : o) : (v[j] < o ? o : v[j]);
-      }
-    }
-    // partners within this thread
-#pragma unroll
-    for (int s = KPT / 2; s >= 1; s /= 2) {
-      if (s < size) {
-#pragma unroll
-        for (int j = 0; j < KPT; ++j) {
-          if (j & s) continue;
-          const bool up = ((tid * KPT + j) & size) == 0;
-          const uint64_t a = v[j], b = v[j | s];
-          if ((a > b) == up) {
-            v[j] = b;
-            v[j | s] = a;
-          }
-        }
-      }
-    }
-  }
+// binary32 estimates for the screen of the admission test, by bit manipulation (no binary64
+// arithmetic): the mantissa is truncated, so the relative error is below 2^-23.
+// x >= 0 (binary64): -1 when x lies outside the normal binary32 range (the screen then defers to
+// binary64).
+__device__ __forceinline__ float approx_f32(double x) {
+  const unsigned long long u = static_cast<unsigned long long>(__double_as_longlong(x));
+  if (u == 0ull) return 0.f;
+  const int e = int(u >> 52) - 1023;
+  if ((u >> 63) || e < -126 || e > 127) return -1.f;
+  return __uint_as_float((uint32_t(e + 127) << 23) | (uint32_t(u >> 29) & 0x7FFFFFu));
 }
 
-template <int KPT>
-__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(ScheduleParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint64_t* keys = reinterpret_cast<uint64_t*>(smem);                       // [n_pad]
-  float* cs = reinterpret_cast<float*>(smem + sizeof(uint64_t) * p.n_pad);  // [N * K], then
-  int32_t* counts = reinterpret_cast<int32_t*>(cs);                          // [N] (reused)
-  __shared__ long long warp_tot[kSchedWarps];
-  __shared__ int32_t s_bstar;
-  __shared__ int32_t s_items;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int32_t NK = p.N * p.K;
-  if (tid == 0) {
-    if (p.status) *p.status = SV_OK;
-    s_bstar = 0x7FFFFFFF;
-    s_items = 0;
-  }
-  for (int32_t i = tid; i < p.n_pad; i += kSchedThreads) keys[i] = ~0ull;
-  for (int32_t i = tid; i < NK; i += kSchedThreads) cs[i] = p.c[i];
-  __syncthreads();
+// T * 2^-40 for 0 <= T < 2^63 (T * 2^-40 then lies in the normal binary32 range, or is 0).
+__device__ __forceinline__ float approx_f32_scaled40(long long T) {
+  if (T <= 0) return 0.f;
+  const int lz = __clzll(T);
+  const unsigned long long norm = static_cast<unsigned long long>(T) << lz;  // leading bit at 63
+  const int e = 63 - lz - 40;
+  return __uint_as_float((uint32_t(e + 127) << 23) | (uint32_t(norm >> 40) & 0x7FFFFFu));
+}
 
-  // 1. survival products and keys
-  int32_t my_items = 0;
-  for (int32_t i = tid; i < p.N; i += kSchedThreads) {
+__device__ __forceinline__ int32_t clamp_len(const ScheduleParams& p, int32_t i) {
+  const int32_t L = p.max_len ? p.max_len[i] : p.K;
+  return (L < 0 || L > p.K) ? 0 : L;
+}
+
+// Number of entries of the ascending array a[0, n) below key (strict) or, with `upper`, not above
+// it: a branch-free lower / upper bound.
+__device__ __forceinline__ int32_t count_below(const uint64_t* a, int32_t n, uint64_t key,
+                                               bool upper) {
+  int32_t pos = 0;
+  int32_t step = 1;
+  while (step * 2 <= n) step *= 2;
+  for (; step >= 1; step >>= 1)
+    if (pos + step <= n) {
+      const uint64_t v = a[pos + step - 1];
+      if (v < key || (upper && v == key)) pos += step;
+    }
+  return pos;
+}
+
+// chunk: CTA c forms the keys of requests [c R, c R + R) -- one ascending run of K keys each, all
+// ones past max_len -- and sorts them by merging the runs pairwise in shared memory (each key's
+// place in the merged pair is its place in its own run plus its count in the partner run).
+__global__ void __launch_bounds__(kChunkThreads) schedule_chunk_kernel(ScheduleParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint64_t* buf[2] = {reinterpret_cast<uint64_t*>(smem),
+                      reinterpret_cast<uint64_t*>(smem) + p.CL};
+  const int tid = threadIdx.x;
+  // the rank kernel may launch now (it waits for this grid's results itself)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // survival products and keys, one thread per request (its probabilities are read sixteen at a
+  // time, ahead of the sequential products)
+  for (int32_t t = tid; t < p.R; t += kChunkThreads) {
+    const int32_t i = blockIdx.x * p.R + t;
+    uint64_t* run = buf[0] + t * p.K;
+    if (i >= p.N) {
+      for (int32_t k = 0; k < p.K; ++k) run[k] = ~0ull;
+      continue;
+    }
     int32_t L = p.max_len ? p.max_len[i] : p.K;
     if (L < 0 || L > p.K) {
       report(p.status, SV_ERR_BAD_INPUT);
       L = 0;
     }
+    const float* ci = p.c + size_t(i) * p.K;
     float S = 1.0f;
-    for (int32_t k = 1; k <= p.K; ++k) {
-      float out = 0.0f;
-      if (k <= L) {
-        const float c = cs[i * p.K + (k - 1)];
-        if (!(c >= 0.0f && c <= 1.0f)) report(p.status, SV_ERR_BAD_INPUT);
-        S = __fmul_rn(S, c);
-        out = S;
-        const uint32_t bits = S == 0.0f ? 0u : __float_as_uint(S);  // -0 ranks as +0
-        keys[i * p.K + (k - 1)] = (uint64_t(~bits) << 32) | (uint64_t(k) << 20) | uint64_t(i);
+    for (int32_t k0 = 0; k0 < p.K; k0 += 16) {
+      float cv[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) cv[u] = k0 + u < L ? __ldg(ci + k0 + u) : 0.0f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int32_t k = k0 + u + 1;
+        if (k > p.K) break;
+        float out = 0.0f;
+        uint64_t key = ~0ull;
+        if (k <= L) {
+          const float c = cv[u];
+          if (!(c >= 0.0f && c <= 1.0f)) report(p.status, SV_ERR_BAD_INPUT);
+          S = __fmul_rn(S, c);
+          out = S;
+          const uint32_t bits = S == 0.0f ? 0u : __float_as_uint(S);  // -0 ranks as +0
+          key = (uint64_t(~bits) << 32) | (uint64_t(k) << 20) | uint64_t(i);
+        }
+        run[k - 1] = key;
+        if (p.survival) p.survival[size_t(i) * p.K + (k - 1)] = out;
       }
-      if (p.survival) p.survival[size_t(i) * p.K + (k - 1)] = out;
     }
-    my_items += L;
   }
+  __syncthreads();
+
+  // merge runs of length w pairwise until one run remains; all-ones keys are equal, so a key of a
+  // left run counts the partner's keys below it and a key of a right run those not above it
+  int src = 0;
+  for (int32_t w = p.K; w < p.CL; w *= 2) {
+    const uint64_t* in = buf[src];
+    uint64_t* out = buf[src ^ 1];
+    for (int32_t e = tid; e < p.CL; e += kChunkThreads) {
+      const int32_t q = e / w;
+      const int32_t pq = q ^ 1;
+      const uint64_t key = in[e];
+      const int32_t lo = min(q, pq) * w;
+      const int32_t p0 = pq * w;
+      const int32_t pn = min(p0 + w, p.CL) - p0;  // partner length (<= 0: no partner)
+      const int32_t own = e - q * w;
+      out[pn > 0 ? lo + own + count_below(in + p0, pn, key, (q & 1) != 0) : e] = key;
+    }
+    __syncthreads();
+    src ^= 1;
+  }
+  uint64_t* dst = p.chunk_keys + size_t(blockIdx.x) * p.CL;
+  for (int32_t e = tid; e < p.CL; e += kChunkThreads) dst[e] = buf[src][e];
+}
+
+// rank: every CTA stages all sorted chunks; the rank of a key is its place in its own chunk plus
+// its count in each other chunk (groups of G lanes split the chunks of one key), and the rank
+// places F = floor(S * 2^40) and the request in sorted order.
+__global__ void __launch_bounds__(kRankThreads) schedule_rank_kernel(ScheduleParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint64_t* keys = reinterpret_cast<uint64_t*>(smem);  // [n_chunks][CL]
+  const int tid = threadIdx.x, lane = tid & 31;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the chunk kernel's results
+  const int32_t total = p.n_chunks * p.CL;
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(p.chunk_keys);
+    uint4* dst = reinterpret_cast<uint4*>(keys);
+    for (int32_t v = tid; v < total / 2; v += kRankThreads) dst[v] = __ldcg(src + v);
+    if ((total & 1) && tid == 0) keys[total - 1] = __ldcg(p.chunk_keys + total - 1);
+  }
+  __syncthreads();
+  int32_t G = 1;  // lanes per key: a power of two, at most 32
+  while (G < p.n_chunks && G < 32) G *= 2;
+  const int32_t gl = lane & (G - 1);          // this lane within its group
+  const int32_t groups = kRankThreads / G;    // keys in flight per CTA
+  const int32_t per = (total + gridDim.x - 1) / gridDim.x;
+  const int32_t e0 = blockIdx.x * per, e1 = min(total, e0 + per);
+  for (int32_t base = e0; base < e1; base += groups) {
+    const int32_t e = base + tid / G;
+    const bool live = e < e1;
+    const uint64_t key = live ? keys[e] : ~0ull;
+    const int32_t own = e / p.CL;
+    int32_t cnt = 0;
+    if (key != ~0ull) {
+      for (int32_t c = gl; c < p.n_chunks; c += G)
+        cnt += c == own ? e - own * p.CL : count_below(keys + c * p.CL, p.CL, key, false);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      if (o < G) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (key != ~0ull && gl == 0) {
+      p.sorted_F[cnt] = fixed40(key);
+      p.sorted_req[cnt] = static_cast<int32_t>(key & 0xFFFFFu);
+    }
+  }
+}
+
+template <int KPT>
+__global__ void __launch_bounds__(kSchedThreads) schedule_admit_kernel(ScheduleParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  int32_t* counts = reinterpret_cast<int32_t*>(smem);  // [N] admitted prefixes per request
+  __shared__ long long warp_tot[kSchedWarps];
+  __shared__ int32_t s_bstar;
+  __shared__ int32_t s_items;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_bstar = 0x7FFFFFFF;
+    s_items = 0;
+  }
+  for (int32_t i = tid; i < p.N; i += kSchedThreads) counts[i] = 0;
+  __syncthreads();
+  // inputs first (they do not depend on the rank kernel): the item count and this thread's SPS
+  int32_t my_items = 0;
+  for (int32_t i = tid; i < p.N; i += kSchedThreads) my_items += clamp_len(p, i);
   atomicAdd(&s_items, my_items);
-  __syncthreads();
-  // per-request counts reuse the staged probabilities (N <= N * K whenever there are items)
-  if (NK > 0)
-    for (int32_t i = tid; i < p.N; i += kSchedThreads) counts[i] = 0;
-
-  // 2. sort
-  uint64_t v[KPT];
+  const int32_t b0 = tid * KPT;  // this thread owns ranks [b0, b0 + KPT)
+  double sp[KPT + 1];
+  const double* spb = p.sps + p.N + b0;
+  if (KPT % 2 == 0 && p.N + b0 + KPT <= p.B_max &&
+      (reinterpret_cast<uintptr_t>(spb) & 15u) == 0) {
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) v[j] = keys[tid * KPT + j];
-  __syncthreads();
-  bitonic_sort<KPT>(v, keys, tid);
-
-  // 3. exact prefix sums of F in sorted order: this thread owns ranks [b0, b0 + KPT)
-  const int32_t n_items = s_items;
-  const int32_t b0 = tid * KPT;
-  long long F[KPT];
-  long long run = 0;
+    for (int j = 0; j + 1 < KPT; j += 2) {
+      const double2 v = __ldg(reinterpret_cast<const double2*>(spb + j));
+      sp[j] = v.x;
+      sp[j + 1] = v.y;
+    }
+    sp[KPT] = __ldg(spb + KPT);
+  } else {
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    F[j] = b0 + j < n_items ? fixed40(v[j]) : 0;
-    run += F[j];
+    for (int j = 0; j <= KPT; ++j) sp[j] = p.N + b0 + j <= p.B_max ? p.sps[p.N + b0 + j] : 0.0;
   }
+  __syncthreads();
+  const int32_t n_items = s_items;
+  // the rank kernel's results
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // exact prefix sums of F in sorted order
+  long long F[KPT];
+  int32_t req[KPT];
+  long long run = 0;
+  if (KPT % 2 == 0 && b0 + KPT <= n_items) {  // whole run: 16-byte loads (b0 a multiple of KPT)
+#pragma unroll
+    for (int j = 0; j + 1 < KPT; j += 2) {
+      const longlong2 v = __ldcg(reinterpret_cast<const longlong2*>(p.sorted_F + b0 + j));
+      F[j] = v.x;
+      F[j + 1] = v.y;
+    }
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) req[j] = __ldcg(p.sorted_req + b0 + j);
+  } else {
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const bool in = b0 + j < n_items;
+      F[j] = in ? __ldcg(p.sorted_F + b0 + j) : 0;
+      req[j] = in ? __ldcg(p.sorted_req + b0 + j) : -1;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) run += F[j];
   long long incl = run;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -194,33 +302,47 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(ScheduleParams 
   const long long base =
       (static_cast<long long>(p.N) << 40) + (warp > 0 ? warp_tot[warp - 1] : 0) + (incl - run);
 
-  // 4. first non-increase of f(b) = T(b) 2^-40 sps[N + b], b < b_lim
+  // first non-increase of f(b) = T(b) 2^-40 sps[N + b], b < b_lim.  A binary32 estimate of both
+  // sides (relative error below 3e-7 each) settles every comparison whose sides differ by more
+  // than 4e-6 relative; the rest are decided in binary64, exactly as defined.
   const int32_t b_lim = min(n_items, p.B_max - p.N);
-  double sp[KPT + 1];
+  float spf[KPT + 1];
 #pragma unroll
-  for (int j = 0; j <= KPT; ++j) sp[j] = b0 + j <= b_lim ? p.sps[p.N + b0 + j] : 0.0;
+  for (int j = 0; j <= KPT; ++j) spf[j] = approx_f32(sp[j]);
   long long T = base;  // T(b0)
+  float Tf = approx_f32_scaled40(T);
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
     const int32_t b = b0 + j;
     if (b < b_lim) {
       const long long Tn = T + F[j];
-      const double f = static_cast<double>(T) * kTwoM40 * sp[j];
-      const double fn = static_cast<double>(Tn) * kTwoM40 * sp[j + 1];
-      if (!(fn > f)) {
+      const float Tnf = approx_f32_scaled40(Tn);
+      const float ff = Tf * spf[j], fnf = Tnf * spf[j + 1];
+      bool up;
+      if (spf[j] >= 0.f && spf[j + 1] >= 0.f && fnf > ff * (1.0f + 4e-6f)) {
+        up = true;
+      } else if (spf[j] >= 0.f && spf[j + 1] >= 0.f && fnf < ff * (1.0f - 4e-6f)) {
+        up = false;
+      } else {
+        const double f = static_cast<double>(T) * kTwoM40 * sp[j];
+        const double fn = static_cast<double>(Tn) * kTwoM40 * sp[j + 1];
+        up = fn > f;
+      }
+      if (!up) {
         atomicMin(&s_bstar, b);
         break;
       }
       T = Tn;
+      Tf = Tnf;
     }
   }
   __syncthreads();
   const int32_t bstar = s_bstar == 0x7FFFFFFF ? max(b_lim, 0) : s_bstar;
 
-  // 5. admitted prefixes per request
+  // admitted prefixes per request (a prefix of its run, by the ordering)
 #pragma unroll
   for (int j = 0; j < KPT; ++j)
-    if (b0 + j < bstar) atomicAdd(&counts[static_cast<int32_t>(v[j] & 0xFFFFFu)], 1);
+    if (b0 + j < bstar) atomicAdd(&counts[req[j]], 1);
   // T(b*): published by the thread owning rank b* - 1 (thread 0 for b* = 0)
   if (bstar == 0) {
     if (tid == 0) {
@@ -237,17 +359,46 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(ScheduleParams 
     *p.objective = static_cast<double>(Tq) * kTwoM40 * p.sps[p.N + bstar];
   }
   __syncthreads();
-  for (int32_t i = tid; i < p.N; i += kSchedThreads) p.sel_len[i] = NK > 0 ? counts[i] : 0;
+  for (int32_t i = tid; i < p.N; i += kSchedThreads) p.sel_len[i] = counts[i];
 }
 
-template <int KPT>
-static cudaError_t launch_schedule(const ScheduleParams& p, size_t smem, cudaStream_t stream) {
-  const void* fn = reinterpret_cast<const void*>(&schedule_kernel<KPT>);
-  const cudaError_t e =
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+// Launches `kernel` as a programmatic dependent of the previous kernel on `stream`.
+template <typename... Args>
+static cudaError_t launch_dependent(void (*kernel)(Args...), unsigned grid, int threads,
+                                    size_t smem, cudaStream_t stream, Args... args) {
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  schedule_kernel<KPT><<<1, kSchedThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+struct ChunkShape {
+  int32_t R, CL, n_chunks;
+};
+
+static ChunkShape chunk_shape(int32_t N, int32_t K) {
+  ChunkShape c;
+  c.R = std::max(1, kChunkSlots / std::max(K, 1));
+  c.CL = c.R * std::max(K, 1);
+  c.n_chunks = std::max(1, (N + c.R - 1) / c.R);
+  return c;
+}
+
+static size_t schedule_ws_bytes(int32_t N, int32_t K) {
+  const ChunkShape c = chunk_shape(N, K);
+  const size_t nk = size_t(std::max<int64_t>(int64_t(N) * K, 1));
+  return align256(sizeof(uint64_t) * size_t(c.n_chunks) * size_t(c.CL)) +
+         align256(sizeof(long long) * nk) + align256(sizeof(int32_t) * nk);
 }
 
 }  // namespace sv
@@ -255,9 +406,8 @@ static cudaError_t launch_schedule(const ScheduleParams& p, size_t smem, cudaStr
 using namespace sv;
 
 extern "C" size_t dspark_schedule_workspace_bytes(int32_t N, int32_t K) {
-  (void)N;
-  (void)K;
-  return 256;  // the scheduler works in shared memory
+  if (N < 0 || K < 0) return 0;
+  return schedule_ws_bytes(N, K);
 }
 
 extern "C" sv_status dspark_schedule(const float* cond_accept, const int32_t* max_len, int32_t N,
@@ -265,28 +415,71 @@ extern "C" sv_status dspark_schedule(const float* cond_accept, const int32_t* ma
                                      int32_t* sel_len, float* survival, int32_t* total_rows,
                                      double* objective, int32_t* status, void* workspace,
                                      size_t workspace_bytes, void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (N < 0 || K < 0 || B_max < N) return SV_ERR_INVALID;
   if (!sel_len || !total_rows || !objective || !sps) return SV_ERR_INVALID;
   if (N > 0 && K > 0 && !cond_accept) return SV_ERR_INVALID;
   if (int64_t(N) * K > kSchedMaxItems || K >= 4096 || N >= (1 << 20)) return SV_ERR_UNSUPPORTED;
-  int32_t n_pad = kSchedThreads;
-  while (n_pad < N * K) n_pad <<= 1;
-  // keys, then the staged probabilities (reused for the per-request counts: N <= N * K whenever
-  // there are items to admit)
-  const size_t cs_bytes = sizeof(float) * size_t(int64_t(N) * K);
-  const size_t smem = sizeof(uint64_t) * size_t(n_pad) + ((cs_bytes + 15) & ~size_t(15));
-  ScheduleParams p{cond_accept, max_len, N, K, sps, B_max, n_pad, sel_len, survival, total_rows,
-                   objective, status};
+  if (!workspace || !aligned256(workspace) || workspace_bytes < schedule_ws_bytes(N, K))
+    return SV_ERR_INVALID;
+  const int32_t NK = N * K;
+  const ChunkShape cs = chunk_shape(N, K);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t keys_bytes = align256(sizeof(uint64_t) * size_t(cs.n_chunks) * size_t(cs.CL));
+  const size_t f_bytes = align256(sizeof(long long) * size_t(NK > 0 ? NK : 1));
+  ScheduleParams p;
+  p.c = cond_accept;
+  p.max_len = max_len;
+  p.N = N;
+  p.K = K;
+  p.sps = sps;
+  p.B_max = B_max;
+  p.sel_len = sel_len;
+  p.survival = survival;
+  p.total_rows = total_rows;
+  p.objective = objective;
+  p.status = status;
+  p.R = cs.R;
+  p.CL = cs.CL;
+  p.n_chunks = cs.n_chunks;
+  p.chunk_keys = reinterpret_cast<uint64_t*>(ws);
+  p.sorted_F = reinterpret_cast<long long*>(ws + keys_bytes);
+  p.sorted_req = reinterpret_cast<int32_t*>(ws + keys_bytes + f_bytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
+  if (status && cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return SV_ERR_CUDA;
+  const int sms = device_sm_count();
+  const int smem_sm = device_smem_per_sm();
+  if (sms <= 0 || smem_sm <= 0) return SV_ERR_CUDA;
+
+  profile_mark(0, s);
+  // chunk: one CTA per chunk of R requests; double-buffered keys
+  const size_t chunk_smem = 2 * sizeof(uint64_t) * size_t(cs.CL);
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&schedule_chunk_kernel),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(chunk_smem));
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  schedule_chunk_kernel<<<unsigned(cs.n_chunks), kChunkThreads, chunk_smem, s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  // rank: every SM (as many CTAs as fit), each staging all chunks
+  const size_t rank_smem = sizeof(uint64_t) * size_t(cs.n_chunks) * size_t(cs.CL);
+  const int per_sm = std::max(1, std::min(4, smem_sm / int(rank_smem + 2048)));
+  const int64_t total = int64_t(cs.n_chunks) * cs.CL;
+  const unsigned rank_grid = unsigned(std::max<int64_t>(
+      1, std::min<int64_t>(int64_t(sms) * per_sm, (total + 63) / 64)));
+  e = launch_dependent(schedule_rank_kernel, rank_grid, kRankThreads, rank_smem, s, p);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  profile_mark(1, s);
+  profile_mark(2, s);
+  // admit: one CTA
+  int32_t n_pad = kSchedThreads;
+  while (n_pad < NK) n_pad <<= 1;
+  const size_t admit_smem = std::max<size_t>(sizeof(int32_t) * size_t(N), 16);
   switch (n_pad / kSchedThreads) {
-    case 1: e = launch_schedule<1>(p, smem, s); break;
-    case 2: e = launch_schedule<2>(p, smem, s); break;
-    case 4: e = launch_schedule<4>(p, smem, s); break;
-    case 8: e = launch_schedule<8>(p, smem, s); break;
-    default: e = launch_schedule<16>(p, smem, s); break;
+    case 1: e = launch_dependent(schedule_admit_kernel<1>, 1, kSchedThreads, admit_smem, s, p); break;
+    case 2: e = launch_dependent(schedule_admit_kernel<2>, 1, kSchedThreads, admit_smem, s, p); break;
+    case 4: e = launch_dependent(schedule_admit_kernel<4>, 1, kSchedThreads, admit_smem, s, p); break;
+    case 8: e = launch_dependent(schedule_admit_kernel<8>, 1, kSchedThreads, admit_smem, s, p); break;
+    default: e = launch_dependent(schedule_admit_kernel<16>, 1, kSchedThreads, admit_smem, s, p); break;
   }
+  profile_mark(3, s);
   return launch_status(e);
 }

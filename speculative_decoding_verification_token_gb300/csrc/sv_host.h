@@ -17,6 +17,9 @@ inline int elem_bytes(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
 // Number of SMs of the current device (queried once per device).
 int device_sm_count();
 
+// Shared memory per SM of the current device, in bytes (queried once per device).
+int device_smem_per_sm();
+
 // Resident CTAs per SM of `kernel` with `smem` bytes of dynamic shared memory (0 on error).
 int resident_ctas(const void* kernel, int threads, size_t smem);
 

@@ -934,15 +934,16 @@ __global__ void __launch_bounds__(kThreads, 4) race_kernel(RaceParams p) {
     bulk_g2s(share_sm, trow + lo * esize<E>(), vec_bytes, &share_bar);
   }
   __syncthreads();
-  if (staged) mbar_wait(&share_bar, 0, p.status);
-  const uint4* vsrc = staged ? reinterpret_cast<const uint4*>(share_sm)
-                             : reinterpret_cast<const uint4*>(trow + lo * esize<E>());
+  const uint4* gsrc = reinterpret_cast<const uint4*>(trow + lo * esize<E>());
 
   // seed: the best exact key among the threads' largest-logit entries, raised to the best seed
   // the job's other shares have published so far -- a lower bound on the winning key, against
-  // which the main pass gates
+  // which the main pass gates.  It reads the share from global memory (L2) while the bulk copy
+  // stages it for the main pass.
   RaceSlot* slot = p.ws.slots + job;
-  float seed = active ? seed_range<E>(rs, vsrc, trow, drow, lo, int32_t(hi - lo)) : -INFINITY;
+  float seed = active ? seed_range<E>(rs, gsrc, trow, drow, lo, int32_t(hi - lo)) : -INFINITY;
+  if (staged) mbar_wait(&share_bar, 0, p.status);
+  const uint4* vsrc = staged ? reinterpret_cast<const uint4*>(share_sm) : gsrc;
   seed = block_max(seed, red_k);
   if (tid == 0) {
     const uint32_t prev = active ? atomicMax(&slot->k0, key_order(seed)) : 0u;

@@ -78,6 +78,8 @@ def _load():
             "orc_markov_draft_request": (C.c_int, [P, i64, P, P, i32, P, P, i32, i64, i32, u64,
                                                    u64, P, P, P, P, P, P]),
             "orc_schedule": (C.c_int, [P, P, i32, i32, P, i32, P, P, P, P]),
+            "orc_schedule_rule": (C.c_int, [P, P, i32, i32, P, i32, i32, P, P, P, P]),
+            "orc_acceptance_update": (C.c_int, [P, P, i32, i32, f64, f64, f64, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -259,7 +261,11 @@ def markov_draft_request(backbone, U, W, anchor, scores, T, seed, req, forced_pr
     return {"status": st, "z": z, "x": x, "stats": stats, "conf": conf, "margin": margin}
 
 
-def schedule(cond_accept, max_len, sps, B_max):
+STOP_FIRST_DROP = 0
+STOP_ARGMAX = 1
+
+
+def schedule(cond_accept, max_len, sps, B_max, rule=STOP_FIRST_DROP):
     c = _f32(cond_accept)
     N, K = c.shape
     ml = _arr(max_len, np.int32)
@@ -268,7 +274,23 @@ def schedule(cond_accept, max_len, sps, B_max):
     surv = np.zeros((N, K), dtype=np.float32)
     total = C.c_int32()
     obj = C.c_double()
-    st = _load().orc_schedule(c.ctypes.data, ml.ctypes.data, N, K, sps.ctypes.data, B_max,
-                              sel.ctypes.data, surv.ctypes.data, C.byref(total), C.byref(obj))
+    st = _load().orc_schedule_rule(c.ctypes.data, ml.ctypes.data, N, K, sps.ctypes.data, B_max,
+                                   int(rule), sel.ctypes.data, surv.ctypes.data, C.byref(total),
+                                   C.byref(obj))
     return {"status": st, "sel_len": sel, "survival": surv, "total_rows": total.value,
             "objective": obj.value}
+
+
+def acceptance_update(sel_len, accepted_len, K, trials, accepts, decay=1.0, prior_a=1.0,
+                      prior_b=1.0):
+    """One round of the per-position acceptance counts (updated in place); returns (status,
+    alpha float32 [K])."""
+    sel = _arr(sel_len, np.int32)
+    acc = _arr(accepted_len, np.int32)
+    assert trials.dtype == np.float64 and accepts.dtype == np.float64
+    assert trials.flags.c_contiguous and accepts.flags.c_contiguous
+    alpha = np.zeros(K, dtype=np.float32)
+    st = _load().orc_acceptance_update(sel.ctypes.data, acc.ctypes.data, sel.size, K,
+                                       float(decay), float(prior_a), float(prior_b),
+                                       trials.ctypes.data, accepts.ctypes.data, alpha.ctypes.data)
+    return st, alpha

@@ -523,10 +523,11 @@ static int item_order(const void* a, const void* b) {
   return 0;
 }
 
-int orc_schedule(const float* cond_accept, const int32_t* max_len, int32_t N, int32_t K,
-                 const double* sps, int32_t B_max, int32_t* sel_len, float* survival,
-                 int32_t* total_rows, double* objective) {
+int orc_schedule_rule(const float* cond_accept, const int32_t* max_len, int32_t N, int32_t K,
+                      const double* sps, int32_t B_max, int32_t rule, int32_t* sel_len,
+                      float* survival, int32_t* total_rows, double* objective) {
   if (N < 0 || K < 0 || B_max < N || !sel_len || !total_rows || !objective) return ORC_ERR_ARGS;
+  if (rule != ORC_STOP_FIRST_DROP && rule != ORC_STOP_ARGMAX) return ORC_ERR_ARGS;
   int64_t n_items = 0;
   for (int32_t i = 0; i < N; ++i) {
     if (max_len[i] < 0 || max_len[i] > K) return ORC_ERR_ARGS;
@@ -559,18 +560,73 @@ int orc_schedule(const float* cond_accept, const int32_t* max_len, int32_t N, in
   int64_t Tb = (int64_t)N << 40; /* one guaranteed token per request, in 2^-40 units */
   double f = (double)Tb * ldexp(1.0, -40) * sps[N];
   int64_t b = 0;
-  while (b < n_items && (int64_t)N + b + 1 <= (int64_t)B_max) {
-    int64_t F = (int64_t)floor((double)items[b].S * two40);
-    int64_t Tn = Tb + F;
-    double fn = (double)Tn * ldexp(1.0, -40) * sps[N + b + 1];
-    if (!(fn > f)) break; /* early stop: never look past the first non-increase */
-    Tb = Tn;
-    f = fn;
-    sel_len[items[b].i] += 1;
-    ++b;
+  if (rule == ORC_STOP_FIRST_DROP) {
+    while (b < n_items && (int64_t)N + b + 1 <= (int64_t)B_max) {
+      int64_t F = (int64_t)floor((double)items[b].S * two40);
+      int64_t Tn = Tb + F;
+      double fn = (double)Tn * ldexp(1.0, -40) * sps[N + b + 1];
+      if (!(fn > f)) break; /* early stop: never look past the first non-increase */
+      Tb = Tn;
+      f = fn;
+      ++b;
+    }
+  } else {
+    /* every admissible budget b = 0 .. min(items, B_max - N); the largest f(b), the smallest b
+       among equals */
+    const int64_t b_lim = n_items < (int64_t)B_max - N ? n_items : (int64_t)B_max - N;
+    double best = f;
+    for (int64_t j = 1; j <= b_lim; ++j) {
+      Tb += (int64_t)floor((double)items[j - 1].S * two40);
+      double fj = (double)Tb * ldexp(1.0, -40) * sps[N + j];
+      if (fj > best) {
+        best = fj;
+        b = j;
+      }
+    }
+    f = best;
   }
+  for (int64_t j = 0; j < b; ++j) sel_len[items[j].i] += 1;
   *total_rows = (int32_t)(N + b);
   *objective = f;
   free(items);
   return ORC_OK;
+}
+
+int orc_schedule(const float* cond_accept, const int32_t* max_len, int32_t N, int32_t K,
+                 const double* sps, int32_t B_max, int32_t* sel_len, float* survival,
+                 int32_t* total_rows, double* objective) {
+  return orc_schedule_rule(cond_accept, max_len, N, K, sps, B_max, ORC_STOP_FIRST_DROP, sel_len,
+                           survival, total_rows, objective);
+}
+
+/* ---- online per-position acceptance ----------------------------------------------------------- */
+
+int orc_acceptance_update(const int32_t* sel_len, const int32_t* accepted_len, int32_t N,
+                          int32_t K, double decay, double prior_a, double prior_b, double* trials,
+                          double* accepts, float* alpha) {
+  if (N < 0 || K < 0 || !trials || !accepts || !alpha) return ORC_ERR_ARGS;
+  if (!(decay >= 0.0 && decay <= 1.0) || !(prior_a > 0.0) || !(prior_b > 0.0)) return ORC_ERR_ARGS;
+  if (N > 0 && (!sel_len || !accepted_len)) return ORC_ERR_ARGS;
+  int bad = 0;
+  for (int32_t k = 1; k <= K; ++k) {
+    /* position k was reached by request i when every earlier drafted token was accepted and k was
+       verified: k <= min(accepted + 1, verified); it was accepted when k <= accepted */
+    int64_t reached = 0, taken = 0;
+    for (int32_t i = 0; i < N; ++i) {
+      const int32_t s = sel_len[i], a = accepted_len[i];
+      if (s < 0 || s > K || a < 0 || a > s) {
+        bad = 1;
+        continue;
+      }
+      const int32_t last = a + 1 < s ? a + 1 : s;
+      if (k <= last) ++reached;
+      if (k <= a) ++taken;
+    }
+    trials[k - 1] = decay * trials[k - 1] + (double)reached;
+    accepts[k - 1] = decay * accepts[k - 1] + (double)taken;
+    /* posterior mean of the conditional acceptance probability under a Beta(prior_a, prior_b)
+       prior */
+    alpha[k - 1] = (float)((accepts[k - 1] + prior_a) / (trials[k - 1] + prior_a + prior_b));
+  }
+  return bad ? ORC_ERR_NAN : ORC_OK;
 }

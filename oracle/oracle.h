@@ -190,6 +190,32 @@ int orc_schedule(const float* cond_accept, const int32_t* max_len, int32_t N, in
                  const double* sps, int32_t B_max, int32_t* sel_len, float* survival,
                  int32_t* total_rows, double* objective);
 
+/* Stopping rules of the scheduler.  FIRST_DROP: the rule above (DSpark's early stop).  ARGMAX: the
+ * budget with the highest expected tokens per unit time over every admissible budget, as [TC]
+ * "Adaptive verification" describes vLLM's choice ("for each possible number of verification rows
+ * b ... picks the budget with the highest result"): b* = the smallest b in 0..min(items, B_max - N)
+ * with f(b) = max f.  The order, F, T and f are the same as above. */
+enum { ORC_STOP_FIRST_DROP = 0, ORC_STOP_ARGMAX = 1 };
+int orc_schedule_rule(const float* cond_accept, const int32_t* max_len, int32_t N, int32_t K,
+                      const double* sps, int32_t B_max, int32_t rule, int32_t* sel_len,
+                      float* survival, int32_t* total_rows, double* objective);
+
+/* Per-position acceptance learned while serving ([TC] "Adaptive verification": without a confidence
+ * head the engine watches what gets accepted and learns how much to trust the drafter at each
+ * position).  Request i verified its first sel_len[i] drafted tokens and accepted the first
+ * accepted_len[i] (0 <= accepted <= verified <= K).  Position k (1-based) was reached when every
+ * earlier token was accepted, k <= min(accepted + 1, verified), and accepted when k <= accepted.
+ * Reading: the counts decay by `decay` in [0, 1] before a round is added, and the estimate of the
+ * conditional acceptance probability is the posterior mean under a Beta(prior_a, prior_b) prior:
+ *   trials[k]  = decay * trials[k]  + #{i : k <= min(accepted_i + 1, verified_i)}
+ *   accepts[k] = decay * accepts[k] + #{i : k <= accepted_i}
+ *   alpha[k]   = (float) ((accepts[k] + prior_a) / (trials[k] + prior_a + prior_b))
+ * trials, accepts: K doubles, updated in place; alpha: K floats.  A request with inconsistent
+ * lengths is skipped and ORC_ERR_NAN returned. */
+int orc_acceptance_update(const int32_t* sel_len, const int32_t* accepted_len, int32_t N,
+                          int32_t K, double decay, double prior_a, double prior_b, double* trials,
+                          double* accepts, float* alpha);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,159 @@
+"""Pins of the oracle's adaptive-verification pieces ("How much does a token cost", "Adaptive
+verification"): the scheduler's budget chosen as the best expected tokens per unit time over every
+budget, and the per-position acceptance rates learned from what verification accepted."""
+import numpy as np
+import pytest
+
+from speculative_decoding_verification_token_gb300 import synth
+
+
+# ---- budget by the highest expected tokens per unit time ----------------------------------------
+
+def _brute_force_argmax(c, max_len, sps, B_max):
+    """Independent restatement in Python: float32 survival products, a tuple sort, exact integer
+    fixed-point sums, and every budget evaluated."""
+    N, K = c.shape
+    items = []
+    for i in range(N):
+        S = np.float32(1.0)
+        for k in range(1, int(max_len[i]) + 1):
+            S = np.float32(S * np.float32(c[i, k - 1]))
+            items.append((-float(S), k, i, float(S)))
+    items.sort()
+    b_lim = min(len(items), B_max - N)
+    T = N << 40
+    best, bstar = float(T) * 2.0 ** -40 * sps[N], 0
+    for b in range(1, b_lim + 1):
+        T += int(np.floor(items[b - 1][3] * 2.0 ** 40))
+        f = float(T) * 2.0 ** -40 * sps[N + b]
+        if f > best:
+            best, bstar = f, b
+    sel = np.zeros(N, np.int32)
+    for _, _, i, _ in items[:bstar]:
+        sel[i] += 1
+    return sel, N + bstar, best
+
+
+def test_argmax_hand_worked_two_peaks(orc):
+    """One request, S = 0.5, 0.5.  f(0) = 1 * 1.0, f(1) = 1.5 * 0.6 = 0.9, f(2) = 2.0 * 0.6 = 1.2:
+    the early stop keeps nothing (f(1) < f(0)); the best budget admits both drafts."""
+    c = np.array([[0.5, 1.0]], np.float32)
+    sps = np.array([0.0, 1.0, 0.6, 0.6])
+    early = orc.schedule(c, [2], sps, 3, rule=orc.STOP_FIRST_DROP)
+    best = orc.schedule(c, [2], sps, 3, rule=orc.STOP_ARGMAX)
+    assert early["status"] == 0 and best["status"] == 0
+    assert early["total_rows"] == 1 and list(early["sel_len"]) == [0]
+    assert abs(early["objective"] - 1.0) < 1e-12
+    assert best["total_rows"] == 3 and list(best["sel_len"]) == [2]
+    assert abs(best["objective"] - 1.2) < 1e-12
+
+
+def test_argmax_ties_take_the_smaller_budget(orc):
+    """f(0) = 1, f(1) = 2 * 0.5 = 1: equal values keep the smaller budget."""
+    c = np.array([[1.0]], np.float32)
+    r = orc.schedule(c, [1], np.array([0.0, 1.0, 0.5]), 2, rule=orc.STOP_ARGMAX)
+    assert r["total_rows"] == 1 and r["objective"] == 1.0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_argmax_matches_brute_force(orc, seed):
+    rng = np.random.default_rng(700 + seed)
+    N, K = int(rng.integers(1, 9)), int(rng.integers(1, 7))
+    c = rng.uniform(0.0, 1.0, (N, K)).astype(np.float32)
+    c[rng.random((N, K)) < 0.1] = 1.0
+    max_len = rng.integers(0, K + 1, N).astype(np.int32)
+    B_max = int(N + rng.integers(0, N * K + 2))
+    # a bumpy SPS curve, so that f has several local maxima
+    sps = 1.0 / (1.0 + 0.05 * np.arange(B_max + 1)) * (1.0 + 0.3 * np.sin(np.arange(B_max + 1)))
+    ref = _brute_force_argmax(c, max_len, sps, B_max)
+    got = orc.schedule(c, max_len, sps, B_max, rule=orc.STOP_ARGMAX)
+    assert got["status"] == 0
+    assert (got["sel_len"] == ref[0]).all()
+    assert got["total_rows"] == ref[1] and got["objective"] == ref[2]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_argmax_dominates_early_stop(orc, seed):
+    """The best budget's objective is never below the early stop's, and both admit a prefix of the
+    same order (per request, the shorter prefixes first)."""
+    rng = np.random.default_rng(800 + seed)
+    N, K = 40, 8
+    c = (rng.beta(8, 2, (N, K)) * 0.97 ** np.arange(K)).astype(np.float32)
+    max_len = rng.integers(0, K + 1, N).astype(np.int32)
+    B_max = N + 200
+    sps = 1.0 / (2e-3 + np.arange(B_max + 1) * rng.uniform(1e-6, 3e-5))
+    sps = sps * (1.0 + 0.02 * rng.standard_normal(B_max + 1))  # a noisy engine profile
+    early = orc.schedule(c, max_len, sps, B_max, rule=orc.STOP_FIRST_DROP)
+    best = orc.schedule(c, max_len, sps, B_max, rule=orc.STOP_ARGMAX)
+    assert best["objective"] >= early["objective"]
+    assert (best["sel_len"] <= max_len).all() and (early["sel_len"] <= max_len).all()
+    assert best["total_rows"] == N + best["sel_len"].sum()
+
+
+def test_argmax_equals_early_stop_when_f_is_log_concave(orc):
+    """With a linear SPS curve, log f(b) = log T(b) + log SPS(N + b) is concave (T grows by
+    non-increasing steps), so the first non-increase is the global maximum."""
+    inp = synth.schedule_inputs(synth.SCHEDULE)
+    N, B_max = inp["N"], inp["B_max"]
+    sps = 500.0 - 0.05 * np.arange(B_max + 1)
+    early = orc.schedule(inp["cond_accept"], inp["max_len"], sps, B_max, rule=orc.STOP_FIRST_DROP)
+    best = orc.schedule(inp["cond_accept"], inp["max_len"], sps, B_max, rule=orc.STOP_ARGMAX)
+    assert early["total_rows"] > N
+    assert (early["sel_len"] == best["sel_len"]).all()
+    assert early["objective"] == best["objective"]
+
+
+# ---- per-position acceptance learned while serving ----------------------------------------------
+
+def test_acceptance_hand_worked(orc):
+    """Three requests, K = 4: verified (4, 2, 3), accepted (1, 2, 3).
+    Reached: request 0 positions 1-2 (rejected at 2), request 1 positions 1-2 (all verified ones
+    accepted), request 2 positions 1-3.  trials = (3, 3, 1, 0), accepts = (3, 2, 1, 0); with a
+    Beta(1, 1) prior alpha = (4/5, 3/5, 2/3, 1/2)."""
+    trials, accepts = np.zeros(4), np.zeros(4)
+    st, alpha = orc.acceptance_update([4, 2, 3], [1, 2, 3], 4, trials, accepts)
+    assert st == 0
+    assert list(trials) == [3, 3, 1, 0] and list(accepts) == [3, 2, 1, 0]
+    np.testing.assert_allclose(alpha, [0.8, 0.6, 2 / 3, 0.5], rtol=1e-7)
+
+
+def test_acceptance_decay_closed_form(orc):
+    """Two rounds with decay 1/2: trials = 1/2 * round 1 + round 2."""
+    trials, accepts = np.zeros(3), np.zeros(3)
+    orc.acceptance_update([3, 3], [3, 0], 3, trials, accepts, decay=0.5)   # (2,1,1) / (1,1,1)
+    st, alpha = orc.acceptance_update([3], [1], 3, trials, accepts, decay=0.5,
+                                      prior_a=2.0, prior_b=3.0)            # (1,1,0) / (1,0,0)
+    assert st == 0
+    np.testing.assert_array_equal(trials, [2.0, 1.5, 0.5])
+    np.testing.assert_array_equal(accepts, [1.5, 0.5, 0.5])
+    np.testing.assert_allclose(alpha, [(1.5 + 2) / (2 + 5), (0.5 + 2) / (1.5 + 5),
+                                       (0.5 + 2) / (0.5 + 5)], rtol=1e-7)
+
+
+def test_acceptance_converges_to_the_conditional_rates(orc):
+    """Token-level verification of synthetic rounds where position k is accepted with probability
+    a_k given that every earlier token was: the estimates converge to a_k (within four standard
+    errors), for any verified lengths."""
+    rng = np.random.default_rng(11)
+    a = np.array([0.9, 0.75, 0.6, 0.5, 0.35])
+    K = a.size
+    trials, accepts = np.zeros(K), np.zeros(K)
+    for _ in range(40):
+        n = 5000
+        sel = rng.integers(0, K + 1, n).astype(np.int32)
+        ok = rng.random((n, K)) < a
+        acc = np.where(ok.all(axis=1), K, np.argmin(ok, axis=1))  # first rejection
+        acc = np.minimum(acc, sel).astype(np.int32)
+        st, alpha = orc.acceptance_update(sel, acc, K, trials, accepts)
+        assert st == 0
+    se = np.sqrt(a * (1 - a) / trials)
+    assert np.all(np.abs(alpha - a) < 4 * se), (alpha, a, se)
+    # the counts can only shrink along the block: reaching k + 1 needs k accepted
+    assert np.all(accepts <= trials) and np.all(trials[1:] <= accepts[:-1])
+
+
+def test_acceptance_inconsistent_lengths(orc):
+    trials, accepts = np.zeros(2), np.zeros(2)
+    st, _ = orc.acceptance_update([1, 2], [2, 1], 2, trials, accepts)  # accepted > verified
+    assert st != 0
+    assert list(trials) == [1, 1] and list(accepts) == [1, 0]           # the bad request skipped

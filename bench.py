@@ -366,6 +366,28 @@ def bench_rows(steps, warmup):
                                "total_rows": int(sched["o"]["total_rows"].item()),
                                "status": int(status.item())}
 
+    # the best-budget rule on the same inputs, and one per-position acceptance update
+    def sch_best():
+        sched["o"] = sv.dspark_schedule(c, ml, sps, si["B_max"], status=status, workspace=sws,
+                                        rule=sv.SV_STOP_ARGMAX)
+    t = time_calls(sch_best, steps, warmup, flush, stream)
+    rows["schedule_best_budget_512x16"] = {
+        "us": sum(t) / len(t) * 1e6, "total_rows": int(sched["o"]["total_rows"].item()),
+        "status": int(status.item())}
+    sel = sched["o"]["sel_len"]
+    acc = torch.minimum(sel, torch.arange(sw.N, device=dev, dtype=torch.int32) % 5)
+    trials = torch.zeros(sw.K, dtype=torch.float64, device=dev)
+    accepts = torch.zeros(sw.K, dtype=torch.float64, device=dev)
+    cond_out = torch.empty((sw.N, sw.K), dtype=torch.float32, device=dev)
+    alpha = torch.empty(sw.K, dtype=torch.float32, device=dev)
+
+    def upd():
+        sv.dspark_acceptance_update(sel, acc, trials, accepts, decay=0.99, alpha=alpha,
+                                    cond_accept_out=cond_out, status=status)
+    t = time_calls(upd, steps, warmup, flush, stream)
+    rows["acceptance_update_512x16"] = {"us": sum(t) / len(t) * 1e6,
+                                        "status": int(status.item())}
+
     # scheduled round: schedule, then verify the selected prefixes (V = 129280)
     vw = synth.SCHEDULED_VERIFY
     vin = synth.token_inputs(vw, device=dev)

@@ -230,6 +230,46 @@ sv_status dspark_schedule(const float* cond_accept, const int32_t* max_len, int3
                           int32_t* total_rows, double* objective, int32_t* status,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* Stopping rules of the scheduler.
+ *   SV_STOP_FIRST_DROP  admit while f still rises and stop at its first non-increase (DSpark's early
+ *                       stop; "DeepSeek DSpark 详解" §04, "DSpark: DeepSeek's bet on speed...").
+ *   SV_STOP_ARGMAX      the budget with the highest expected tokens per unit time over every
+ *                       admissible budget b = 0 .. min(items, B_max - N), the smallest b among
+ *                       equals (vLLM's choice in "How much does a token cost", "Adaptive
+ *                       verification"). */
+typedef enum { SV_STOP_FIRST_DROP = 0, SV_STOP_ARGMAX = 1 } sv_stop_rule;
+
+/* dspark_schedule with a choice of stopping rule (`rule`, an sv_stop_rule); the order, the fixed
+ * point sums and f(b) are those of dspark_schedule, and so are the arguments, outputs, errors and
+ * workspace (dspark_schedule_workspace_bytes).  dspark_schedule is rule SV_STOP_FIRST_DROP. */
+sv_status dspark_schedule_rule(const float* cond_accept, const int32_t* max_len, int32_t N,
+                               int32_t K, const double* sps, int32_t B_max, int32_t rule,
+                               int32_t* sel_len, float* survival, int32_t* total_rows,
+                               double* objective, int32_t* status, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* Per-position acceptance learned while serving ("How much does a token cost", "Adaptive
+ * verification": a drafter without a confidence head gets a per-position trust level estimated
+ * from the tokens verification accepted).  One verified round: request i verified its first
+ * sel_len[i] drafted tokens and accepted the first accepted_len[i] (DEVICE int32 [N] each, the
+ * scheduler's and the verifier's outputs).  Position k (1-based) was reached iff
+ * k <= min(accepted + 1, verified), accepted iff k <= accepted; the counts decay by `decay`
+ * (in [0, 1]; 1 keeps every round) before the round is added:
+ *   trials[k]  = decay * trials[k]  + #{i : k <= min(accepted_i + 1, verified_i)}
+ *   accepts[k] = decay * accepts[k] + #{i : k <= accepted_i}
+ *   alpha[k]   = (float) ((accepts[k] + prior_a) / (trials[k] + prior_a + prior_b))
+ * the posterior mean of the conditional acceptance probability under a Beta(prior_a, prior_b)
+ * prior (prior_a, prior_b > 0).  trials, accepts: DEVICE fp64 [K], read and updated in place (the
+ * caller zeroes them once); alpha: DEVICE fp32 [K]; cond_accept_out (nullable): DEVICE fp32 [N][K],
+ * every row set to alpha -- the next round's dspark_schedule input for a drafter without a
+ * confidence head.  1 <= K < 4096 (K = 0: nothing to do).  A request with inconsistent lengths
+ * (accepted > verified, verified outside [0, K]) is skipped and SV_ERR_BAD_INPUT written to
+ * `status`.  No workspace. */
+sv_status dspark_acceptance_update(const int32_t* sel_len, const int32_t* accepted_len, int32_t N,
+                                   int32_t K, double decay, double prior_a, double prior_b,
+                                   double* trials, double* accepts, float* alpha,
+                                   float* cond_accept_out, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -191,18 +191,18 @@ int orc_schedule(const float* cond_accept, const int32_t* max_len, int32_t N, in
                  int32_t* total_rows, double* objective);
 
 /* Stopping rules of the scheduler.  FIRST_DROP: the rule above (DSpark's early stop).  ARGMAX: the
- * budget with the highest expected tokens per unit time over every admissible budget, as [TC]
- * "Adaptive verification" describes vLLM's choice ("for each possible number of verification rows
- * b ... picks the budget with the highest result"): b* = the smallest b in 0..min(items, B_max - N)
- * with f(b) = max f.  The order, F, T and f are the same as above. */
+ * budget with the highest expected tokens per unit time over every admissible budget, vLLM's choice
+ * in [TC] "Adaptive verification" (each budget filled with the positions most likely to survive,
+ * the best one kept): b* = the smallest b in 0..min(items, B_max - N) with f(b) = max f.  The order,
+ * F, T and f are the same as above. */
 enum { ORC_STOP_FIRST_DROP = 0, ORC_STOP_ARGMAX = 1 };
 int orc_schedule_rule(const float* cond_accept, const int32_t* max_len, int32_t N, int32_t K,
                       const double* sps, int32_t B_max, int32_t rule, int32_t* sel_len,
                       float* survival, int32_t* total_rows, double* objective);
 
-/* Per-position acceptance learned while serving ([TC] "Adaptive verification": without a confidence
- * head the engine watches what gets accepted and learns how much to trust the drafter at each
- * position).  Request i verified its first sel_len[i] drafted tokens and accepted the first
+/* Per-position acceptance learned while serving ([TC] "Adaptive verification": a drafter without a
+ * confidence head gets a per-position trust level estimated from the tokens verification
+ * accepted).  Request i verified its first sel_len[i] drafted tokens and accepted the first
  * accepted_len[i] (0 <= accepted <= verified <= K).  Position k (1-based) was reached when every
  * earlier token was accepted, k <= min(accepted + 1, verified), and accepted when k <= accepted.
  * Reading: the counts decay by `decay` in [0, 1] before a round is added, and the estimate of the

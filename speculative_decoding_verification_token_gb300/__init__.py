@@ -69,6 +69,9 @@ def lib():
                                          P, P, i64, P, P, P, P, sz, P]),
             "dspark_schedule_workspace_bytes": (sz, [i32, i32]),
             "dspark_schedule": (st, [P, P, i32, i32, P, i32, P, P, P, P, P, P, sz, P]),
+            "dspark_schedule_rule": (st, [P, P, i32, i32, P, i32, i32, P, P, P, P, P, P, sz, P]),
+            "dspark_acceptance_update": (st, [P, P, i32, i32, C.c_double, C.c_double, C.c_double,
+                                              P, P, P, P, P, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -291,9 +294,14 @@ def dspark_schedule_workspace_bytes(N, K):
     return int(lib().dspark_schedule_workspace_bytes(N, K))
 
 
+SV_STOP_FIRST_DROP = 0
+SV_STOP_ARGMAX = 1
+
+
 def dspark_schedule(cond_accept, max_len, sps, B_max, want_survival=True, status=None,
-                    workspace=None, stream=None):
-    """Hardware-aware prefix scheduler.  cond_accept fp32 [N, K]; sps fp64 [B_max + 1]."""
+                    workspace=None, stream=None, rule=SV_STOP_FIRST_DROP):
+    """Hardware-aware prefix scheduler.  cond_accept fp32 [N, K]; sps fp64 [B_max + 1]; rule:
+    SV_STOP_FIRST_DROP (early stop) or SV_STOP_ARGMAX (best budget over all)."""
     _dev(cond_accept, torch.float32), _dev(max_len, torch.int32), _dev(sps, torch.float64)
     N, K = cond_accept.shape
     dev = cond_accept.device
@@ -305,9 +313,35 @@ def dspark_schedule(cond_accept, max_len, sps, B_max, want_survival=True, status
         status = torch.zeros(1, dtype=torch.int32, device=dev)
     need = dspark_schedule_workspace_bytes(N, K)
     ws = workspace if workspace is not None else globals()["workspace"](need, dev)
-    code = lib().dspark_schedule(_ptr(cond_accept), _ptr(max_len), N, K, _ptr(sps), int(B_max),
-                                 _ptr(sel), _ptr(surv), _ptr(total), _ptr(obj), _ptr(status),
-                                 _ptr(ws), ws.numel(), _stream(stream))
-    _check(code, "dspark_schedule")
+    code = lib().dspark_schedule_rule(_ptr(cond_accept), _ptr(max_len), N, K, _ptr(sps),
+                                      int(B_max), int(rule), _ptr(sel), _ptr(surv), _ptr(total),
+                                      _ptr(obj), _ptr(status), _ptr(ws), ws.numel(),
+                                      _stream(stream))
+    _check(code, "dspark_schedule_rule")
     return {"sel_len": sel, "survival": surv, "total_rows": total, "objective": obj,
             "status": status}
+
+
+def dspark_acceptance_update(sel_len, accepted_len, trials, accepts, decay=1.0, prior_a=1.0,
+                             prior_b=1.0, alpha=None, cond_accept_out=None, status=None,
+                             stream=None):
+    """One verified round into the per-position acceptance counts (fp64 [K] device tensors,
+    updated in place).  Returns {"alpha": fp32 [K], "cond_accept": fp32 [N, K] or None,
+    "status"}."""
+    _dev(sel_len, torch.int32), _dev(accepted_len, torch.int32)
+    _dev(trials, torch.float64), _dev(accepts, torch.float64)
+    N = sel_len.numel()
+    K = trials.numel()
+    if accepts.numel() != K or accepted_len.numel() != N:
+        raise ValueError("inconsistent sizes")
+    dev = trials.device
+    if alpha is None:
+        alpha = torch.empty(K, dtype=torch.float32, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    code = lib().dspark_acceptance_update(_ptr(sel_len), _ptr(accepted_len), N, K, float(decay),
+                                          float(prior_a), float(prior_b), _ptr(trials),
+                                          _ptr(accepts), _ptr(alpha), _ptr(cond_accept_out),
+                                          _ptr(status), _stream(stream))
+    _check(code, "dspark_acceptance_update")
+    return {"alpha": alpha, "cond_accept": cond_accept_out, "status": status}

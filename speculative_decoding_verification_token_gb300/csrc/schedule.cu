@@ -45,6 +45,7 @@ struct ScheduleParams {
   int32_t* total_rows;
   double* objective;
   int32_t* status;
+  int32_t rule;           // SV_STOP_FIRST_DROP or SV_STOP_ARGMAX
   int32_t R;              // requests per chunk
   int32_t CL;             // keys per chunk (R * K)
   int32_t n_chunks;       // ceil(N / R)
@@ -226,10 +227,14 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_admit_kernel(ScheduleP
   __shared__ long long warp_tot[kSchedWarps];
   __shared__ int32_t s_bstar;
   __shared__ int32_t s_items;
+  __shared__ uint32_t s_fmax;            // argmax rule: largest binary32 estimate (bits)
+  __shared__ unsigned long long s_fbest;  // argmax rule: largest exact f among candidates (bits)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_bstar = 0x7FFFFFFF;
     s_items = 0;
+    s_fmax = 0u;
+    s_fbest = 0ull;
   }
   for (int32_t i = tid; i < p.N; i += kSchedThreads) counts[i] = 0;
   __syncthreads();
@@ -302,39 +307,92 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_admit_kernel(ScheduleP
   const long long base =
       (static_cast<long long>(p.N) << 40) + (warp > 0 ? warp_tot[warp - 1] : 0) + (incl - run);
 
-  // first non-increase of f(b) = T(b) 2^-40 sps[N + b], b < b_lim.  A binary32 estimate of both
-  // sides (relative error below 3e-7 each) settles every comparison whose sides differ by more
-  // than 4e-6 relative; the rest are decided in binary64, exactly as defined.
   const int32_t b_lim = min(n_items, p.B_max - p.N);
   float spf[KPT + 1];
 #pragma unroll
   for (int j = 0; j <= KPT; ++j) spf[j] = approx_f32(sp[j]);
-  long long T = base;  // T(b0)
-  float Tf = approx_f32_scaled40(T);
+  if (p.rule == SV_STOP_FIRST_DROP) {
+    // first non-increase of f(b) = T(b) 2^-40 sps[N + b], b < b_lim.  A binary32 estimate of both
+    // sides (relative error below 3e-7 each) settles every comparison whose sides differ by more
+    // than 4e-6 relative; the rest are decided in binary64, exactly as defined.
+    long long T = base;  // T(b0)
+    float Tf = approx_f32_scaled40(T);
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    const int32_t b = b0 + j;
-    if (b < b_lim) {
-      const long long Tn = T + F[j];
-      const float Tnf = approx_f32_scaled40(Tn);
-      const float ff = Tf * spf[j], fnf = Tnf * spf[j + 1];
-      bool up;
-      if (spf[j] >= 0.f && spf[j + 1] >= 0.f && fnf > ff * (1.0f + 4e-6f)) {
-        up = true;
-      } else if (spf[j] >= 0.f && spf[j + 1] >= 0.f && fnf < ff * (1.0f - 4e-6f)) {
-        up = false;
-      } else {
-        const double f = static_cast<double>(T) * kTwoM40 * sp[j];
-        const double fn = static_cast<double>(Tn) * kTwoM40 * sp[j + 1];
-        up = fn > f;
+    for (int j = 0; j < KPT; ++j) {
+      const int32_t b = b0 + j;
+      if (b < b_lim) {
+        const long long Tn = T + F[j];
+        const float Tnf = approx_f32_scaled40(Tn);
+        const float ff = Tf * spf[j], fnf = Tnf * spf[j + 1];
+        bool up;
+        if (spf[j] >= 0.f && spf[j + 1] >= 0.f && fnf > ff * (1.0f + 4e-6f)) {
+          up = true;
+        } else if (spf[j] >= 0.f && spf[j + 1] >= 0.f && fnf < ff * (1.0f - 4e-6f)) {
+          up = false;
+        } else {
+          const double f = static_cast<double>(T) * kTwoM40 * sp[j];
+          const double fn = static_cast<double>(Tn) * kTwoM40 * sp[j + 1];
+          up = fn > f;
+        }
+        if (!up) {
+          atomicMin(&s_bstar, b);
+          break;
+        }
+        T = Tn;
+        Tf = Tnf;
       }
-      if (!up) {
-        atomicMin(&s_bstar, b);
+    }
+  } else {
+    // the largest f(b) over b = 0 .. b_lim, the smallest b among equals.  This thread owns the
+    // budgets b0 + 1 .. b0 + KPT (and thread 0 also b = 0).  The binary32 estimates (relative
+    // error below 3e-7) leave as candidates only budgets within 8e-6 of the largest estimate,
+    // which always include the true maximum; the candidates compare in binary64.
+    // budget b0 + j (j = 1 .. KPT) at index j, and b = 0 at index 0 on thread 0; an estimate of
+    // -1 marks a budget out of range, `force` one whose SPS lies outside the binary32 range
+    long long Tb[KPT + 1];
+    float fe[KPT + 1];
+    bool force[KPT + 1];
+    Tb[0] = base;
+    fe[0] = -1.f;
+    force[0] = false;
+    if (tid == 0) {
+      force[0] = !(spf[0] >= 0.f);
+      fe[0] = force[0] ? -1.f : approx_f32_scaled40(base) * spf[0];
+    }
+    long long T = base;
+#pragma unroll
+    for (int j = 1; j <= KPT; ++j) {
+      T += F[j - 1];
+      Tb[j] = T;
+      const bool in = b0 + j <= b_lim;
+      force[j] = in && !(spf[j] >= 0.f);
+      fe[j] = in && !force[j] ? approx_f32_scaled40(T) * spf[j] : -1.f;
+    }
+    float m = -1.f;
+#pragma unroll
+    for (int j = 0; j <= KPT; ++j) m = fmaxf(m, fe[j]);
+    m = warp_max(m);
+    if (lane == 0 && m >= 0.f) atomicMax(&s_fmax, __float_as_uint(m));  // order-preserving for >= 0
+    __syncthreads();
+    const float cut = __uint_as_float(s_fmax) * (1.0f - 8e-6f);
+    double fx[KPT + 1];
+    bool cand[KPT + 1];
+#pragma unroll
+    for (int j = 0; j <= KPT; ++j) {
+      cand[j] = force[j] || (fe[j] >= 0.f && fe[j] >= cut);
+      fx[j] = cand[j] ? static_cast<double>(Tb[j]) * kTwoM40 * sp[j] : 0.0;
+    }
+#pragma unroll
+    for (int j = 0; j <= KPT; ++j)  // f >= 0: the bit pattern orders as the value
+      if (cand[j]) atomicMax(&s_fbest, static_cast<unsigned long long>(__double_as_longlong(fx[j])));
+    __syncthreads();
+    const double fbest = __longlong_as_double(static_cast<long long>(s_fbest));
+#pragma unroll
+    for (int j = 0; j <= KPT; ++j)
+      if (cand[j] && fx[j] == fbest) {
+        atomicMin(&s_bstar, j == 0 ? 0 : b0 + j);
         break;
       }
-      T = Tn;
-      Tf = Tnf;
-    }
   }
   __syncthreads();
   const int32_t bstar = s_bstar == 0x7FFFFFFF ? max(b_lim, 0) : s_bstar;
@@ -410,11 +468,12 @@ extern "C" size_t dspark_schedule_workspace_bytes(int32_t N, int32_t K) {
   return schedule_ws_bytes(N, K);
 }
 
-extern "C" sv_status dspark_schedule(const float* cond_accept, const int32_t* max_len, int32_t N,
-                                     int32_t K, const double* sps, int32_t B_max,
-                                     int32_t* sel_len, float* survival, int32_t* total_rows,
-                                     double* objective, int32_t* status, void* workspace,
-                                     size_t workspace_bytes, void* stream) {
+extern "C" sv_status dspark_schedule_rule(const float* cond_accept, const int32_t* max_len,
+                                          int32_t N, int32_t K, const double* sps, int32_t B_max,
+                                          int32_t rule, int32_t* sel_len, float* survival,
+                                          int32_t* total_rows, double* objective, int32_t* status,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (rule != SV_STOP_FIRST_DROP && rule != SV_STOP_ARGMAX) return SV_ERR_INVALID;
   if (N < 0 || K < 0 || B_max < N) return SV_ERR_INVALID;
   if (!sel_len || !total_rows || !objective || !sps) return SV_ERR_INVALID;
   if (N > 0 && K > 0 && !cond_accept) return SV_ERR_INVALID;
@@ -438,6 +497,7 @@ extern "C" sv_status dspark_schedule(const float* cond_accept, const int32_t* ma
   p.total_rows = total_rows;
   p.objective = objective;
   p.status = status;
+  p.rule = rule;
   p.R = cs.R;
   p.CL = cs.CL;
   p.n_chunks = cs.n_chunks;
@@ -482,4 +542,99 @@ extern "C" sv_status dspark_schedule(const float* cond_accept, const int32_t* ma
   }
   profile_mark(3, s);
   return launch_status(e);
+}
+
+extern "C" sv_status dspark_schedule(const float* cond_accept, const int32_t* max_len, int32_t N,
+                                     int32_t K, const double* sps, int32_t B_max,
+                                     int32_t* sel_len, float* survival, int32_t* total_rows,
+                                     double* objective, int32_t* status, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  return dspark_schedule_rule(cond_accept, max_len, N, K, sps, B_max, SV_STOP_FIRST_DROP, sel_len,
+                              survival, total_rows, objective, status, workspace,
+                              workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------------------------------------
+// dspark_acceptance_update: per-position acceptance counts from one verified round
+// ---------------------------------------------------------------------------------------------
+namespace sv {
+
+constexpr int kAcceptThreads = 1024;
+
+struct AcceptParams {
+  const int32_t* sel_len;
+  const int32_t* accepted_len;
+  int32_t N, K;
+  double decay, prior_a, prior_b;
+  double* trials;
+  double* accepts;
+  float* alpha;
+  float* cond_out;
+  int32_t* status;
+};
+
+// One CTA.  Position k was reached by request i iff k <= min(accepted + 1, verified) and accepted
+// iff k <= accepted, so both counts are suffix sums of two histograms (of min(accepted + 1,
+// verified) and of accepted) built with shared-memory atomics.  Then one thread per position
+// updates its counts and estimate, with the same binary64 operations and order as the definition
+// (no fused multiply-add), and the estimates are broadcast to every request's row of cond_out.
+__global__ void __launch_bounds__(kAcceptThreads) acceptance_kernel(AcceptParams p) {
+  extern __shared__ __align__(16) int32_t hist[];  // [2][K + 1], then alpha [K] as floats
+  int32_t* h_last = hist;
+  int32_t* h_acc = hist + (p.K + 1);
+  float* al = reinterpret_cast<float*>(hist + 2 * (p.K + 1));
+  const int tid = threadIdx.x;
+  for (int32_t k = tid; k < 2 * (p.K + 1); k += kAcceptThreads) hist[k] = 0;
+  __syncthreads();
+  for (int32_t i = tid; i < p.N; i += kAcceptThreads) {
+    const int32_t s = p.sel_len[i], a = p.accepted_len[i];
+    if (s < 0 || s > p.K || a < 0 || a > s) {
+      report(p.status, SV_ERR_BAD_INPUT);
+      continue;
+    }
+    atomicAdd(&h_last[min(a + 1, s)], 1);
+    atomicAdd(&h_acc[a], 1);
+  }
+  __syncthreads();
+  for (int32_t k = tid + 1; k <= p.K; k += kAcceptThreads) {
+    int32_t reached = 0, taken = 0;
+    for (int32_t j = k; j <= p.K; ++j) {
+      reached += h_last[j];
+      taken += h_acc[j];
+    }
+    const double t = __dadd_rn(__dmul_rn(p.decay, p.trials[k - 1]), static_cast<double>(reached));
+    const double c = __dadd_rn(__dmul_rn(p.decay, p.accepts[k - 1]), static_cast<double>(taken));
+    p.trials[k - 1] = t;
+    p.accepts[k - 1] = c;
+    const float e = __double2float_rn(
+        __ddiv_rn(__dadd_rn(c, p.prior_a), __dadd_rn(__dadd_rn(t, p.prior_a), p.prior_b)));
+    p.alpha[k - 1] = e;
+    al[k - 1] = e;
+  }
+  if (!p.cond_out) return;
+  __syncthreads();
+  const int64_t NK = int64_t(p.N) * p.K;
+  for (int64_t e = tid; e < NK; e += kAcceptThreads) p.cond_out[e] = al[e % p.K];
+}
+
+}  // namespace sv
+
+extern "C" sv_status dspark_acceptance_update(const int32_t* sel_len,
+                                              const int32_t* accepted_len, int32_t N, int32_t K,
+                                              double decay, double prior_a, double prior_b,
+                                              double* trials, double* accepts, float* alpha,
+                                              float* cond_accept_out, int32_t* status,
+                                              void* stream) {
+  if (N < 0 || K <= 0 || K >= 4096) return K == 0 && N >= 0 ? SV_OK : SV_ERR_INVALID;
+  if (!(decay >= 0.0 && decay <= 1.0) || !(prior_a > 0.0) || !(prior_b > 0.0))
+    return SV_ERR_INVALID;
+  if (!trials || !accepts || !alpha || (N > 0 && (!sel_len || !accepted_len)))
+    return SV_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (status && cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return SV_ERR_CUDA;
+  AcceptParams p{sel_len, accepted_len, N, K, decay, prior_a, prior_b, trials, accepts, alpha,
+                 cond_accept_out, status};
+  const size_t smem = sizeof(int32_t) * size_t(2 * (K + 1)) + sizeof(float) * size_t(K);
+  acceptance_kernel<<<1, kAcceptThreads, smem, s>>>(p);
+  return launch_status(cudaGetLastError());
 }

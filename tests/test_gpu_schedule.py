@@ -103,3 +103,132 @@ def test_scheduled_round(sv, orc):
     lay = layout_np(vin)
     res = compare_verify(gpu, ref, 0, lay["draft_len"], lay["draft_row0"])
     print(f"\n[parity] scheduled round: {res}")
+
+
+# ---- adaptive verification: best-budget rule and learned per-position acceptance ---------------
+
+def _gpu_schedule_rule(sv, c, max_len, sps, B_max, rule):
+    out = sv.dspark_schedule(torch.from_numpy(np.ascontiguousarray(c)).cuda(),
+                             torch.from_numpy(np.ascontiguousarray(max_len, np.int32)).cuda(),
+                             torch.from_numpy(np.ascontiguousarray(sps, np.float64)).cuda(), B_max,
+                             rule=rule)
+    torch.cuda.synchronize()
+    assert int(out["status"].item()) == 0
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_schedule_argmax_rule_matches_oracle(sv, orc, seed):
+    """Best budget over all budgets, bit-exact, on random tables with a bumpy SPS curve (several
+    local maxima of f) and ties."""
+    rng = np.random.default_rng(900 + seed)
+    N = int(rng.integers(1, 700))
+    K = int(rng.integers(1, 20))
+    if N * K > 16384:
+        N = 16384 // K
+    c = (rng.beta(8, 2, (N, K)) * 0.97 ** np.arange(K)).astype(np.float32)
+    c[rng.random((N, K)) < 0.05] = 1.0
+    if N > 2:
+        c[1::3] = c[0:N - 1:3][: len(c[1::3])]
+    max_len = rng.integers(0, K + 1, N).astype(np.int32)
+    B_max = int(N + rng.integers(0, 3 * N * K // 4 + 2))
+    b = np.arange(B_max + 1)
+    sps = 1.0 / (2e-3 + b * rng.uniform(1e-8, 1e-4)) * (1.0 + 0.05 * np.sin(0.3 * b))
+    ref = orc.schedule(c, max_len, sps, B_max, rule=orc.STOP_ARGMAX)
+    assert ref["status"] == 0
+    got = _gpu_schedule_rule(sv, c, max_len, sps, B_max, sv.SV_STOP_ARGMAX)
+    assert (got["sel_len"] == ref["sel_len"]).all()
+    assert int(got["total_rows"][0]) == ref["total_rows"]
+    assert got["objective"][0] == ref["objective"]
+
+
+def test_schedule_argmax_rule_workload_and_edges(sv, orc):
+    inp = synth.schedule_inputs(synth.SCHEDULE)
+    for rule in (sv.SV_STOP_ARGMAX, sv.SV_STOP_FIRST_DROP):
+        ref = orc.schedule(inp["cond_accept"], inp["max_len"], inp["sps"], inp["B_max"],
+                           rule=rule)
+        got = _gpu_schedule_rule(sv, inp["cond_accept"], inp["max_len"], inp["sps"],
+                                 inp["B_max"], rule)
+        assert (got["sel_len"] == ref["sel_len"]).all() and got["objective"][0] == ref["objective"]
+    c = np.array([[0.5, 1.0]], np.float32)                     # two peaks: f = 1, 0.9, 1.2
+    got = _gpu_schedule_rule(sv, c, [2], np.array([0.0, 1.0, 0.6, 0.6]), 3, sv.SV_STOP_ARGMAX)
+    assert int(got["total_rows"][0]) == 3 and list(got["sel_len"]) == [2]
+    c1 = np.array([[1.0]], np.float32)                         # tie f(0) = f(1): the smaller b
+    got = _gpu_schedule_rule(sv, c1, [1], np.array([0.0, 1.0, 0.5]), 2, sv.SV_STOP_ARGMAX)
+    assert int(got["total_rows"][0]) == 1
+    got = _gpu_schedule_rule(sv, c1, [0], np.array([0.0, 1.0, 0.5]), 2, sv.SV_STOP_ARGMAX)
+    assert int(got["total_rows"][0]) == 1                      # nothing extendable
+
+
+def test_acceptance_update_matches_oracle(sv, orc):
+    """Several rounds with decay and a Beta(2, 3) prior: counts and estimates bit-exact, the
+    estimates broadcast to every request's row, and a bad round reported."""
+    rng = np.random.default_rng(31)
+    N, K = 777, 13
+    t_ref, a_ref = np.zeros(K), np.zeros(K)
+    t_dev = torch.zeros(K, dtype=torch.float64, device="cuda")
+    a_dev = torch.zeros(K, dtype=torch.float64, device="cuda")
+    cond = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    for rnd in range(4):
+        sel = rng.integers(0, K + 1, N).astype(np.int32)
+        acc = np.minimum(rng.geometric(0.3, N) - 1, sel).astype(np.int32)
+        st, alpha = orc.acceptance_update(sel, acc, K, t_ref, a_ref, decay=0.9, prior_a=2.0,
+                                          prior_b=3.0)
+        assert st == 0
+        out = sv.dspark_acceptance_update(torch.from_numpy(sel).cuda(), torch.from_numpy(acc).cuda(),
+                                          t_dev, a_dev, decay=0.9, prior_a=2.0, prior_b=3.0,
+                                          cond_accept_out=cond)
+        torch.cuda.synchronize()
+        assert int(out["status"].item()) == 0
+        assert (t_dev.cpu().numpy() == t_ref).all() and (a_dev.cpu().numpy() == a_ref).all()
+        assert (out["alpha"].cpu().numpy().view(np.uint32) == alpha.view(np.uint32)).all()
+        assert (cond.cpu().numpy() == alpha[None, :]).all()
+    bad_sel = torch.tensor([2, 1], dtype=torch.int32, device="cuda")
+    bad_acc = torch.tensor([1, 2], dtype=torch.int32, device="cuda")  # accepted > verified
+    out = sv.dspark_acceptance_update(bad_sel, bad_acc, t_dev[:2].clone(), a_dev[:2].clone())
+    torch.cuda.synchronize()
+    assert int(out["status"].item()) == sv.SV_ERR_BAD_INPUT
+
+
+def test_adaptive_round_on_device(sv, orc):
+    """Learned acceptance -> best-budget schedule -> token verification -> acceptance update,
+    chained on the device with no host round trip, against the same chain in the oracle."""
+    N, K = 48, 8
+    rng = np.random.default_rng(5)
+    # a previous round's outcome seeds the counts (the drafter has no confidence head)
+    sel0 = np.full(N, K, np.int32)
+    acc0 = np.minimum(rng.geometric(0.25, N) - 1, K).astype(np.int32)
+    t_ref, a_ref = np.zeros(K), np.zeros(K)
+    _, alpha = orc.acceptance_update(sel0, acc0, K, t_ref, a_ref)
+    cond_ref = np.repeat(alpha[None, :], N, axis=0)
+    B_max = N * (K + 1)
+    sps = 1.0 / (2e-3 + np.arange(B_max + 1) * 2e-5)
+    ref_s = orc.schedule(cond_ref, np.full(N, K, np.int32), sps, B_max, rule=orc.STOP_ARGMAX)
+    vw = synth.scaled(synth.SCHEDULED_VERIFY, B=N, gamma=K, V=20000)
+    vin = synth.token_inputs(vw, device="cpu")
+    tokens = oracle_tokens(orc, vin)
+    vref_in = dict(vin, draft_len=torch.from_numpy(ref_s["sel_len"]))
+    ref_v = oracle_verify(orc, 0, vref_in, tokens)
+    st, alpha1 = orc.acceptance_update(ref_s["sel_len"], ref_v["accepted_len"], K, t_ref, a_ref)
+    assert st == 0
+
+    t_dev = torch.zeros(K, dtype=torch.float64, device="cuda")
+    a_dev = torch.zeros(K, dtype=torch.float64, device="cuda")
+    cond = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    sv.dspark_acceptance_update(torch.from_numpy(sel0).cuda(), torch.from_numpy(acc0).cuda(),
+                                t_dev, a_dev, cond_accept_out=cond)
+    sched = sv.dspark_schedule(cond, torch.full((N,), K, dtype=torch.int32, device="cuda"),
+                               torch.from_numpy(sps).cuda(), B_max, rule=sv.SV_STOP_ARGMAX)
+    d = {k: vin[k].cuda() for k in ("target", "draft", "target_row0", "draft_row0")}
+    ver = sv.spec_verify_token(d["target"], d["draft"], d["target_row0"], d["draft_row0"],
+                               sched["sel_len"], K, torch.from_numpy(tokens).cuda(), vin["seed"])
+    upd = sv.dspark_acceptance_update(sched["sel_len"], ver["accepted_len"], t_dev, a_dev)
+    torch.cuda.synchronize()
+    assert int(ver["status"].item()) == 0 and int(upd["status"].item()) == 0
+    assert (sched["sel_len"].cpu().numpy() == ref_s["sel_len"]).all()
+    lay = layout_np(vref_in)
+    res = compare_verify(ver, ref_v, 0, lay["draft_len"], lay["draft_row0"])
+    if res["exempt_mismatch"] == 0:
+        assert (t_dev.cpu().numpy() == t_ref).all() and (a_dev.cpu().numpy() == a_ref).all()
+        assert (upd["alpha"].cpu().numpy() == alpha1).all()
+    print(f"\n[parity] adaptive round: {res}")

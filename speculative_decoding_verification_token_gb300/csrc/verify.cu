@@ -39,7 +39,9 @@ constexpr uint32_t kItemBytes = kStagesPerItem * kRowBytes;
 constexpr int kRing = 3;                         // stages of 2 x kRowBytes (target + draft)
 constexpr int kRedBufs = 4;                      // items a consumer warp may run ahead, plus one
 constexpr size_t kStreamSmem = size_t(kRing) * 2 * kRowBytes;
-constexpr int kRaceSplitMax = 8;                 // CTAs (row shares) per race job
+constexpr int kRaceSplitMax = 8;                 // CTAs (row shares) per race job, many jobs
+constexpr int kRaceSplitFew = 16;                // the same when one wave holds every share
+constexpr int kRaceCtasPerSm = 4;                // resident race CTAs per SM (launch bounds)
 constexpr uint32_t kRaceShareMax = 64 * 1024;    // largest row share staged in shared memory
 
 struct RaceDesc {  // per request, written by decide, read by race
@@ -864,7 +866,7 @@ struct RaceParams {
 };
 
 template <typename E>
-__global__ void __launch_bounds__(kThreads, 4) race_kernel(RaceParams p) {
+__global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) race_kernel(RaceParams p) {
   extern __shared__ __align__(128) uint8_t share_sm[];  // this CTA's share of the row (staged)
   __shared__ uint64_t share_bar;
   __shared__ float red_k[kWarps];
@@ -1019,7 +1021,19 @@ struct CommonArgs {
 };
 
 // CTAs per race job for rows of S 16 KB slices: each owns one contiguous share of the row.
-static int32_t race_split(int32_t S) { return std::max(1, std::min(kRaceSplitMax, S)); }
+// When the jobs times kRaceSplitMax shares fit in one wave of resident race CTAs, the shares are
+// made as many as still fit (up to kRaceSplitFew), so that no SM holds more work than it must;
+// otherwise kRaceSplitMax shares per job.
+static int32_t race_split(int32_t S, int64_t jobs) {
+  int32_t cl = kRaceSplitMax;
+  const int sms = device_sm_count();
+  if (sms > 0 && jobs > 0) {
+    const int64_t slots = int64_t(sms) * kRaceCtasPerSm;
+    if (jobs * kRaceSplitMax <= slots)
+      cl = int32_t(std::min<int64_t>(kRaceSplitFew, slots / jobs));
+  }
+  return std::max(1, std::min(cl, S));
+}
 
 static sv_status check_common(const CommonArgs& a, bool need_target) {
   if (a.dtype != SV_F32 && a.dtype != SV_BF16) return SV_ERR_INVALID;
@@ -1069,7 +1083,7 @@ static sv_status launch_block(const BlockParams& bp, cudaStream_t stream) {
 template <typename E>
 static sv_status launch_race(RaceParams rp, int64_t jobs, cudaStream_t stream) {
   if (jobs == 0) return SV_OK;
-  rp.CL = race_split(rp.S);
+  rp.CL = race_split(rp.S, jobs);
   // the kernel's share: ceil(V / (CL * kPer)) whole vectors
   constexpr int64_t kPer = Elem<E>::kPerVec;
   const int64_t share_bytes = (rp.V + rp.CL * kPer - 1) / (rp.CL * kPer) * 16;

@@ -80,6 +80,7 @@ def _load():
             "orc_schedule": (C.c_int, [P, P, i32, i32, P, i32, P, P, P, P]),
             "orc_schedule_rule": (C.c_int, [P, P, i32, i32, P, i32, i32, P, P, P, P]),
             "orc_acceptance_update": (C.c_int, [P, P, i32, i32, f64, f64, f64, P, P, P]),
+            "orc_sts_fit": (C.c_int, [P, P, P, i32, i32, i32, f64, f64, i32, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -294,3 +295,19 @@ def acceptance_update(sel_len, accepted_len, K, trials, accepts, decay=1.0, prio
                                        float(decay), float(prior_a), float(prior_b),
                                        trials.ctypes.data, accepts.ctypes.data, alpha.ctypes.data)
     return st, alpha
+
+
+def sts_fit(scores, sel_len, accepted_len, iters=30, beta_min=1.0 / 16, beta_max=16.0, nbins=15):
+    """Per-position temperatures fitted to the verified outcomes; returns a dict of per-position
+    arrays (T, nll, ece_raw, ece_fit, count) and the status."""
+    s = _f32(scores)
+    N, K = s.shape
+    sel = _arr(sel_len, np.int32)
+    acc = _arr(accepted_len, np.int32)
+    T = np.zeros(K, np.float32)
+    nll, er, ef = np.zeros(K), np.zeros(K), np.zeros(K)
+    cnt = np.zeros(K, np.int32)
+    st = _load().orc_sts_fit(s.ctypes.data, sel.ctypes.data, acc.ctypes.data, N, K, int(iters),
+                             float(beta_min), float(beta_max), int(nbins), T.ctypes.data,
+                             nll.ctypes.data, er.ctypes.data, ef.ctypes.data, cnt.ctypes.data)
+    return {"status": st, "T": T, "nll": nll, "ece_raw": er, "ece_fit": ef, "count": cnt}

@@ -630,3 +630,88 @@ int orc_acceptance_update(const int32_t* sel_len, const int32_t* accepted_len, i
   }
   return bad ? ORC_ERR_NAN : ORC_OK;
 }
+
+/* ---- sequential temperature scaling: fit and calibration error ------------------------------ */
+
+static double logistic(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* log(1 + exp(x)) without overflow */
+static double softplus(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
+
+int orc_sts_fit(const float* scores, const int32_t* sel_len, const int32_t* accepted_len,
+                int32_t N, int32_t K, int32_t iters, double beta_min, double beta_max,
+                int32_t nbins, float* T_out, double* nll_out, double* ece_raw_out,
+                double* ece_fit_out, int32_t* count_out) {
+  if (N < 0 || K < 0 || iters < 0 || nbins <= 0 || !T_out) return ORC_ERR_ARGS;
+  if (!(beta_min > 0.0) || !(beta_max >= beta_min)) return ORC_ERR_ARGS;
+  if (N > 0 && (!scores || !sel_len || !accepted_len)) return ORC_ERR_ARGS;
+  int bad = 0;
+  for (int32_t i = 0; i < N; ++i) {
+    const int32_t s = sel_len[i], a = accepted_len[i];
+    if (s < 0 || s > K || a < 0 || a > s) bad = 1;
+  }
+  double* bin_gap = (double*)malloc(sizeof(double) * (size_t)nbins);
+  for (int32_t k = 1; k <= K; ++k) {
+    /* the samples of position k: requests that reached it (every earlier drafted token accepted,
+       k verified); the label says whether it was accepted */
+    int32_t n = 0;
+    for (int32_t i = 0; i < N; ++i) {
+      const int32_t s = sel_len[i], a = accepted_len[i];
+      if (s < 0 || s > K || a < 0 || a > s) continue;
+      if (k <= (a + 1 < s ? a + 1 : s)) ++n;
+    }
+    /* Newton's method on the convex negative log-likelihood in beta = 1 / T:
+         NLL(beta) = sum_i softplus(-(2 y_i - 1) beta s_i)
+         g = sum_i (sigma(beta s_i) - y_i) s_i,  H = sum_i sigma(beta s_i) (1 - sigma(beta s_i)) s_i^2
+       starting from beta = 1, each step clamped to [beta_min, beta_max] */
+    double beta = 1.0;
+    for (int32_t t = 0; t < iters; ++t) {
+      double g = 0.0, H = 0.0;
+      for (int32_t i = 0; i < N; ++i) {
+        const int32_t s = sel_len[i], a = accepted_len[i];
+        if (s < 0 || s > K || a < 0 || a > s) continue;
+        if (!(k <= (a + 1 < s ? a + 1 : s))) continue;
+        const double x = (double)scores[(int64_t)i * K + (k - 1)];
+        const double y = k <= a ? 1.0 : 0.0;
+        const double q = logistic(beta * x);
+        g += (q - y) * x;
+        H += q * (1.0 - q) * x * x;
+      }
+      if (!(H > 0.0)) break;
+      double nb = beta - g / H;
+      if (nb < beta_min) nb = beta_min;
+      if (nb > beta_max) nb = beta_max;
+      beta = nb;
+    }
+    T_out[k - 1] = (float)(1.0 / beta);
+    /* the fitted loss and the expected calibration error (equal-width bins over [0, 1]:
+       sum over bins of |sum (label - confidence)|, over the samples) before and after */
+    double nll = 0.0;
+    for (int pass = 0; pass < 2; ++pass) {
+      const double b = pass == 0 ? 1.0 : beta;
+      for (int32_t j = 0; j < nbins; ++j) bin_gap[j] = 0.0;
+      for (int32_t i = 0; i < N; ++i) {
+        const int32_t s = sel_len[i], a = accepted_len[i];
+        if (s < 0 || s > K || a < 0 || a > s) continue;
+        if (!(k <= (a + 1 < s ? a + 1 : s))) continue;
+        const double x = (double)scores[(int64_t)i * K + (k - 1)];
+        const double y = k <= a ? 1.0 : 0.0;
+        const double q = logistic(b * x);
+        int32_t bin = (int32_t)floor(q * nbins);
+        if (bin >= nbins) bin = nbins - 1;
+        if (bin < 0) bin = 0;
+        bin_gap[bin] += y - q;
+        if (pass == 1) nll += softplus(-(2.0 * y - 1.0) * b * x);
+      }
+      double ece = 0.0;
+      for (int32_t j = 0; j < nbins; ++j) ece += fabs(bin_gap[j]);
+      ece = n > 0 ? ece / n : 0.0;
+      if (pass == 0 && ece_raw_out) ece_raw_out[k - 1] = ece;
+      if (pass == 1 && ece_fit_out) ece_fit_out[k - 1] = ece;
+    }
+    if (nll_out) nll_out[k - 1] = n > 0 ? nll / n : 0.0;
+    if (count_out) count_out[k - 1] = n;
+  }
+  free(bin_gap);
+  return bad ? ORC_ERR_NAN : ORC_OK;
+}

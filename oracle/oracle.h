@@ -216,6 +216,24 @@ int orc_acceptance_update(const int32_t* sel_len, const int32_t* accepted_len, i
                           int32_t K, double decay, double prior_a, double prior_b, double* trials,
                           double* accepts, float* alpha);
 
+/* Sequential temperature scaling ([KC] "The Second Ace", [DS] §04: one temperature per draft
+ * position divides the confidence head's logit, argmax-preserving, fitted until the stated
+ * confidences match the observed acceptance; the calibration error is the expected calibration
+ * error, ECE).  The samples of position k (1-based) are the requests that reached it (every earlier
+ * drafted token accepted and k verified: k <= min(accepted_len + 1, sel_len)); the label is 1 when
+ * k <= accepted_len.  scores: N*K floats, the confidence logits s.
+ * Reading (the pages give no fitting rule): the standard temperature-scaling fit -- minimise the
+ * negative log-likelihood of sigma(s / T_k) -- by `iters` Newton steps in beta = 1 / T from beta = 1,
+ * each clamped to [beta_min, beta_max], in binary64; ECE over `nbins` equal-width confidence bins:
+ * sum over bins of |sum of (label - confidence)| / n_k.
+ * Outputs per position: T_out (float), nll_out (mean NLL at the fit), ece_raw_out (T = 1),
+ * ece_fit_out, count_out (n_k); all but T_out nullable.  Inconsistent lengths: request skipped,
+ * ORC_ERR_NAN returned. */
+int orc_sts_fit(const float* scores, const int32_t* sel_len, const int32_t* accepted_len,
+                int32_t N, int32_t K, int32_t iters, double beta_min, double beta_max,
+                int32_t nbins, float* T_out, double* nll_out, double* ece_raw_out,
+                double* ece_fit_out, int32_t* count_out);
+
 #ifdef __cplusplus
 }
 #endif

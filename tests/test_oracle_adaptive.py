@@ -157,3 +157,86 @@ def test_acceptance_inconsistent_lengths(orc):
     st, _ = orc.acceptance_update([1, 2], [2, 1], 2, trials, accepts)  # accepted > verified
     assert st != 0
     assert list(trials) == [1, 1] and list(accepts) == [1, 0]           # the bad request skipped
+
+
+# ---- sequential temperature scaling ---------------------------------------------------------------
+
+def _sequential_round(rng, N, K, Tstar, score_std=2.0, verified=None):
+    """Confidence logits s and one verified round whose position-k outcome, given every earlier
+    token accepted, is Bernoulli(sigma(s / Tstar_k))."""
+    s = rng.normal(0.0, score_std, (N, K)).astype(np.float32)
+    p = 1.0 / (1.0 + np.exp(-s.astype(np.float64) / np.asarray(Tstar)))
+    ok = rng.random((N, K)) < p
+    acc = np.where(ok.all(axis=1), K, np.argmin(ok, axis=1)).astype(np.int32)
+    sel = np.full(N, K, np.int32) if verified is None else verified
+    return s, sel, np.minimum(acc, sel).astype(np.int32)
+
+
+def test_sts_recovers_known_temperatures(orc):
+    """Outcomes drawn with temperatures (0.7, 1, 1.5, 2.5): each fitted T is within four standard
+    errors of the true one (Fisher information of beta = 1 / T at the fit)."""
+    rng = np.random.default_rng(21)
+    Tstar = np.array([0.7, 1.0, 1.5, 2.5])
+    s, sel, acc = _sequential_round(rng, 40000, 4, Tstar)
+    r = orc.sts_fit(s, sel, acc)
+    assert r["status"] == 0
+    for k in range(4):
+        reach = np.minimum(acc + 1, sel) >= k + 1
+        x = s[reach, k].astype(np.float64)
+        q = 1.0 / (1.0 + np.exp(-x / r["T"][k]))
+        se_beta = 1.0 / np.sqrt(np.sum(q * (1 - q) * x * x))
+        assert abs(1.0 / r["T"][k] - 1.0 / Tstar[k]) < 4 * se_beta, (k, r["T"][k], Tstar[k])
+        assert r["count"][k] == reach.sum()
+    assert np.all(r["ece_fit"][[0, 2, 3]] < r["ece_raw"][[0, 2, 3]])  # miscalibrated positions
+
+
+def test_sts_matches_a_library_minimiser(orc):
+    """The Newton fit equals scipy's bounded scalar minimisation of the same likelihood."""
+    from scipy.optimize import minimize_scalar
+    rng = np.random.default_rng(22)
+    s, sel, acc = _sequential_round(rng, 3000, 3, [0.8, 1.3, 2.0],
+                                    verified=rng.integers(0, 4, 3000).astype(np.int32))
+    r = orc.sts_fit(s, sel, acc, iters=50)
+    for k in range(3):
+        reach = np.minimum(acc + 1, sel) >= k + 1
+        x = s[reach, k].astype(np.float64)
+        y = (acc[reach] >= k + 1).astype(np.float64)
+
+        def nll(beta):
+            z = -(2 * y - 1) * beta * x
+            return np.sum(np.logaddexp(0.0, z))
+        best = minimize_scalar(nll, bounds=(1 / 16, 16), method="bounded",
+                               options={"xatol": 1e-10})
+        assert abs(1.0 / r["T"][k] - best.x) < 1e-6 * best.x
+        assert abs(r["nll"][k] - best.fun / reach.sum()) < 1e-9
+
+
+def test_sts_calibrated_input_keeps_unit_temperature(orc):
+    rng = np.random.default_rng(23)
+    s, sel, acc = _sequential_round(rng, 60000, 2, [1.0, 1.0])
+    r = orc.sts_fit(s, sel, acc)
+    assert np.all(np.abs(r["T"] - 1.0) < 0.05)
+    assert np.all(r["ece_raw"] < 0.02)
+
+
+def test_sts_ece_hand_worked(orc):
+    """Four samples at position 1 with confidences 1/4, 1/4, 3/4, 3/4 and labels 0, 1, 1, 1, two
+    bins: |(0 - 1/4) + (1 - 1/4)| + |(1 - 3/4) + (1 - 3/4)| = 1, over 4 samples: 0.25."""
+    s = np.array([[np.log(1 / 3)], [np.log(1 / 3)], [np.log(3)], [np.log(3)]], np.float32)
+    sel = np.ones(4, np.int32)
+    acc = np.array([0, 1, 1, 1], np.int32)
+    r = orc.sts_fit(s, sel, acc, iters=0, nbins=2)
+    assert r["T"][0] == 1.0 and r["count"][0] == 4
+    assert abs(r["ece_raw"][0] - 0.25) < 1e-7 and r["ece_fit"][0] == r["ece_raw"][0]
+
+
+def test_sts_preserves_the_order_of_confidences(orc):
+    """Dividing by a positive temperature keeps every position's ranking of the scores."""
+    rng = np.random.default_rng(24)
+    s, sel, acc = _sequential_round(rng, 5000, 3, [0.5, 2.0, 4.0])
+    T = orc.sts_fit(s, sel, acc)["T"]
+    assert np.all(T > 0)
+    for k in range(3):
+        order = np.argsort(s[:, k], kind="stable")
+        c = 1.0 / (1.0 + np.exp(-s[order, k].astype(np.float64) / float(T[k])))
+        assert np.all(np.diff(c) >= 0.0)

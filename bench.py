@@ -388,6 +388,20 @@ def bench_rows(steps, warmup):
     rows["acceptance_update_512x16"] = {"us": sum(t) / len(t) * 1e6,
                                         "status": int(status.item())}
 
+    # temperature fit of the confidence head over 64 verified rounds of 512 requests x 16
+    rng = np.random.default_rng(5)
+    n_cal = 64 * sw.N
+    scores = torch.from_numpy(rng.normal(0.0, 2.0, (n_cal, sw.K)).astype(np.float32)).to(dev)
+    cal_sel = torch.full((n_cal,), sw.K, dtype=torch.int32, device=dev)
+    cal_acc = torch.from_numpy((rng.geometric(0.3, n_cal) - 1).clip(0, sw.K).astype(np.int32)).to(dev)
+    fit = {}
+
+    def sts():
+        fit["o"] = sv.dspark_sts_fit(scores, cal_sel, cal_acc, status=status)
+    t = time_calls(sts, max(3, steps // 3), warmup, flush, stream)
+    rows["sts_fit_32768x16"] = {"us": sum(t) / len(t) * 1e6, "newton_steps": 30,
+                                "status": int(status.item())}
+
     # scheduled round: schedule, then verify the selected prefixes (V = 129280)
     vw = synth.SCHEDULED_VERIFY
     vin = synth.token_inputs(vw, device=dev)

@@ -270,6 +270,25 @@ sv_status dspark_acceptance_update(const int32_t* sel_len, const int32_t* accept
                                    double* trials, double* accepts, float* alpha,
                                    float* cond_accept_out, int32_t* status, void* stream);
 
+/* Sequential temperature scaling of the confidence head ("DeepSeek Boosts Inference Speed by 85%",
+ * "The Second Ace"; "DeepSeek DSpark 详解" §04): one temperature T_k per draft position, dividing
+ * the confidence logit (argmax-preserving), fitted to verified outcomes.  The samples of position k
+ * (1-based) are the requests that reached it, k <= min(accepted_len + 1, sel_len); the label is 1
+ * when k <= accepted_len.  Fit (a reading: the pages give no rule): `iters` Newton steps on the
+ * negative log-likelihood of sigma(s / T_k) in beta = 1 / T_k from beta = 1, each clamped to
+ * [beta_min, beta_max]; the logistic in binary32, the sums in binary64.  Expected calibration error
+ * over `nbins` (1..256) equal-width confidence bins: sum over bins of |sum (label - confidence)|,
+ * over the sample count, at T = 1 (ece_raw_out) and at the fit (ece_fit_out).
+ * scores: DEVICE fp32 [N][K] confidence logits; sel_len, accepted_len: DEVICE int32 [N].
+ * Outputs (DEVICE, per position): T_out fp32 [K]; nll_out fp64 [K] (mean loss at the fit),
+ * ece_raw_out, ece_fit_out fp64 [K], count_out int32 [K] -- all but T_out nullable.
+ * Inconsistent lengths: the request is skipped and SV_ERR_BAD_INPUT written to `status`.
+ * One CTA per position; no workspace. */
+sv_status dspark_sts_fit(const float* scores, const int32_t* sel_len, const int32_t* accepted_len,
+                         int32_t N, int32_t K, int32_t iters, double beta_min, double beta_max,
+                         int32_t nbins, float* T_out, double* nll_out, double* ece_raw_out,
+                         double* ece_fit_out, int32_t* count_out, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

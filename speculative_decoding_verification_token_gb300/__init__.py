@@ -72,6 +72,8 @@ def lib():
             "dspark_schedule_rule": (st, [P, P, i32, i32, P, i32, i32, P, P, P, P, P, P, sz, P]),
             "dspark_acceptance_update": (st, [P, P, i32, i32, C.c_double, C.c_double, C.c_double,
                                               P, P, P, P, P, P]),
+            "dspark_sts_fit": (st, [P, P, P, i32, i32, i32, C.c_double, C.c_double, i32, P, P, P,
+                                    P, P, P, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -345,3 +347,27 @@ def dspark_acceptance_update(sel_len, accepted_len, trials, accepts, decay=1.0, 
                                           _ptr(status), _stream(stream))
     _check(code, "dspark_acceptance_update")
     return {"alpha": alpha, "cond_accept": cond_accept_out, "status": status}
+
+
+def dspark_sts_fit(scores, sel_len, accepted_len, iters=30, beta_min=1.0 / 16, beta_max=16.0,
+                   nbins=15, status=None, stream=None):
+    """Per-position temperatures of the confidence head fitted to verified outcomes (scores fp32
+    [N, K], sel_len / accepted_len int32 [N], all on the device).  Returns device tensors T [K],
+    nll, ece_raw, ece_fit (fp64 [K]), count (int32 [K]) and status."""
+    _dev(scores, torch.float32), _dev(sel_len, torch.int32), _dev(accepted_len, torch.int32)
+    N, K = scores.shape
+    dev = scores.device
+    out = {"T": torch.empty(K, dtype=torch.float32, device=dev),
+           "nll": torch.empty(K, dtype=torch.float64, device=dev),
+           "ece_raw": torch.empty(K, dtype=torch.float64, device=dev),
+           "ece_fit": torch.empty(K, dtype=torch.float64, device=dev),
+           "count": torch.empty(K, dtype=torch.int32, device=dev),
+           "status": status if status is not None else torch.zeros(1, dtype=torch.int32,
+                                                                   device=dev)}
+    code = lib().dspark_sts_fit(_ptr(scores), _ptr(sel_len), _ptr(accepted_len), N, K,
+                                int(iters), float(beta_min), float(beta_max), int(nbins),
+                                _ptr(out["T"]), _ptr(out["nll"]), _ptr(out["ece_raw"]),
+                                _ptr(out["ece_fit"]), _ptr(out["count"]), _ptr(out["status"]),
+                                _stream(stream))
+    _check(code, "dspark_sts_fit")
+    return out

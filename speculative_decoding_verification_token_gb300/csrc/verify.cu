@@ -435,11 +435,15 @@ struct BlockParams {
   const uint64_t* request_ids;
   float* rho_out;  // rho_i per drafted row (nullable)
   float* h_out;    // h_i per drafted row (nullable; non-null computes every R_i)
+  int32_t* accepted_len;
+  int32_t* out_tokens;
+  int64_t out_ld;
+  int32_t* correction_token;
   VerifyWs ws;
   int32_t* status;
 };
 
-enum : int32_t { kSegStats = 0, kSegResid = 1, kSegEnd = 2, kSegExit = 3 };
+enum : int32_t { kSegStats = 0, kSegResid = 1, kSegEnd = 2, kSegExit = 3, kSegRace = 4 };
 
 struct BlockMeta {
   int32_t kind;  // kSeg*
@@ -468,6 +472,9 @@ struct BlockState {  // the request in flight, in shared memory
   float dep[kRedBufs][kConsumerWarps][4];
   int32_t count[kRedBufs];       // warps that have deposited a segment
   int32_t bad;                   // data error seen in the request in flight
+  RaceDesc desc;                 // the decision: tau, residual or bonus, gap
+  uint32_t desc_seq;             // request number whose desc is published
+  uint32_t race_k0;              // key_order of the best exact key of the race so far (0: none)
 };
 
 // Wait until the request number in `w` reaches `seq` (bounded; SV_ERR_TIMEOUT on expiry).
@@ -538,6 +545,39 @@ __device__ void block_producer(const BlockParams& p, uint8_t* ring, uint64_t* fu
     ++seg;
     return true;
   };
+  // the correction (or bonus) row of the decided request: row pair tau + 1, or target row gamma + 1
+  auto issue_race = [&](int32_t r, const RaceDesc& d) {
+    const uint8_t* trow = row_ptr<E>(p.target, p.target_row0[r] + d.tau, p.ld);
+    const uint8_t* drow = d.resid ? row_ptr<E>(p.draft, p.draft_row0[r] + d.tau, p.ld) : nullptr;
+    for (int64_t e0 = 0; e0 < p.V; e0 += kSE) {
+      uint32_t stage;
+      if (!acquire(stage)) return false;
+      BlockMeta m;
+      m.kind = kSegRace;
+      m.row = d.tau + 1;
+      m.last = e0 + kSE >= p.V;
+      m.len = static_cast<int32_t>(p.V - e0 < kSE ? p.V - e0 : kSE);
+      const uint32_t bulk_bytes = (uint32_t(m.len) * esize<E>()) & ~15u;
+      m.bulk = static_cast<int32_t>(bulk_bytes / esize<E>());
+      m.seg = seg;
+      m.r = r;
+      m.seq = seq;
+      m.e0 = e0;
+      m.trow = trow;
+      m.drow = drow;
+      meta[stage] = m;
+      uint8_t* dst = ring + size_t(stage) * 2 * kRowBytes;
+      fence_proxy_async();
+      mbar_expect_tx(&full[stage], (drow ? 2 : 1) * bulk_bytes);
+      if (bulk_bytes) {
+        bulk_g2s(dst, trow + e0 * esize<E>(), bulk_bytes, &full[stage]);
+        if (drow) bulk_g2s(dst + kRowBytes, drow + e0 * esize<E>(), bulk_bytes, &full[stage]);
+      }
+      ++n;
+    }
+    ++seg;
+    return true;
+  };
   auto issue_marker = [&](int32_t kind, int32_t r) {
     uint32_t stage;
     if (!acquire(stage)) return false;
@@ -565,6 +605,9 @@ __device__ void block_producer(const BlockParams& p, uint8_t* ring, uint64_t* fu
       }
     }
     if (!issue_marker(kSegEnd, r)) return;
+    if (!wait_seq(&bs->desc_seq, seq, p.status)) return;
+    const RaceDesc d = bs->desc;
+    if (!issue_race(r, d)) return;
   }
   issue_marker(kSegExit, -1);
 }
@@ -611,7 +654,7 @@ __device__ __forceinline__ float2 resid_vec(float2 acc, const uint4& a, const ui
 // The decision of request r, by one warp once every segment of the request is merged: thresholds
 // h_i, the accepted length tau = max{i : eta_i <= h_i} (0 if none), the race descriptor.
 template <typename E>
-__device__ void block_decide(const BlockParams& p, int32_t r, BlockState* bs) {
+__device__ void block_decide(const BlockParams& p, int32_t r, uint32_t seq, BlockState* bs) {
   if ((threadIdx.x & 31) != 0) return;
   const int32_t graw = p.draft_len[r];
   const int32_t g = clamp_gamma(graw, p.gmax);
@@ -636,9 +679,136 @@ __device__ void block_decide(const BlockParams& p, int32_t r, BlockState* bs) {
   d.resid = tau < g;
   d.gap = d.resid ? resid_gap(bs->norm[tau + 1], tau > 0 ? logf(bs->rho[tau]) : 0.f) : 0.f;
   d.pad = 0;
-  p.ws.desc[r] = d;
   if (graw != g || bs->bad) report(p.status, SV_ERR_BAD_INPUT);
   bs->bad = 0;
+  bs->desc = d;
+  bs->race_k0 = 0u;
+  publish_seq(&bs->desc_seq, seq);  // the producer may stream the race's row now
+}
+
+// ---- the correction (or bonus) race of a decided request, streamed through the ring ----------
+
+// Offers entry e (logit t, draft logit d, Philox word w) to this thread's race if its noise can lift
+// it to the bound (gate constant c = 23 - K0 log2e; see gate_threshold).
+__device__ __forceinline__ void race_offer_td(const RaceSpec& rs, int64_t e, float t, float d,
+                                              uint32_t w, float c, float& bk, int32_t& bi) {
+  if (!(gate_m(w) <= gate_threshold(t, c))) return;
+  if (!race_active(rs, t, d)) return;
+  const float k = race_key(rs, t, d, race_noise(uniform_of(w)));
+  if (race_better(k, int32_t(e), bk, bi)) {
+    bk = k;
+    bi = int32_t(e);
+  }
+}
+
+// Exact key of entry e (-inf if it carries no weight).
+__device__ __forceinline__ float race_exact_td(const RaceSpec& rs, int64_t e, float t, float d) {
+  if (!race_active(rs, t, d)) return -INFINITY;
+  const uint4 b = stream_block(rs.st, static_cast<uint32_t>(e >> 2));
+  return race_key(rs, t, d, race_noise(uniform_of(word_of(b, static_cast<uint32_t>(e & 3)))));
+}
+
+// Seed of one stage: the exact key of this thread's largest-logit entry among its whole vectors.
+template <typename E>
+__device__ float race_stage_seed(const RaceSpec& rs, const uint4* vt, const uint4* vd, int nvec,
+                                 int64_t e0, int tid, int32_t& idx) {
+  constexpr int kPer = Elem<E>::kPerVec;
+  float bt = -INFINITY;
+  int bv = -1;
+  for (int v = tid; v < nvec; v += kConsumers) {
+    const float m = vec_max<E>(vt[v]);
+    if (m > bt) {
+      bt = m;
+      bv = v;
+    }
+  }
+  idx = -1;
+  if (bv < 0) return -INFINITY;
+  float x[8], y[8];
+  Elem<E>::unpack(vt[bv], x);
+  if (rs.resid) Elem<E>::unpack(vd[bv], y);
+  int q0 = 0;
+#pragma unroll
+  for (int q = kPer - 1; q >= 0; --q)
+    if (x[q] == bt) q0 = q;
+  const int64_t e = e0 + int64_t(bv) * kPer + q0;
+  idx = int32_t(e);
+  return race_exact_td(rs, e, bt, rs.resid ? y[q0] : 0.f);
+}
+
+// Main pass of one stage against the bound K0: vectors whose largest logit cannot reach K0 are
+// skipped before any Philox; the others are gated by their largest Philox word, then entry by
+// entry (the race kernel's gate, with the draft logits at hand in the stage).
+template <typename E>
+__device__ void race_stage_main(const RaceSpec& rs, const uint4* vt, const uint4* vd, int nvec,
+                                int32_t len, int64_t e0, const uint8_t* trow,
+                                const uint8_t* drow, int tid, float K0, float& bk, int32_t& bi) {
+  constexpr int kPer = Elem<E>::kPerVec;
+  const float floor_t = K0 - kMaxNoise;
+  const float c = 23.0f - K0 * kLog2e;
+  for (int v = tid; v < nvec; v += kConsumers) {
+    const uint4 a = vt[v];
+    const float tmax = vec_max<E>(a);
+    if (!(tmax >= floor_t)) continue;
+    const int64_t e = e0 + int64_t(v) * kPer;  // a multiple of kPer: whole Philox blocks
+    const uint4 b0 = stream_block(rs.st, static_cast<uint32_t>(e >> 2));
+    const uint4 b1 = kPer == 8 ? stream_block(rs.st, static_cast<uint32_t>(e >> 2) + 1) : b0;
+    const uint32_t wmax = max(max(max(b0.x, b0.y), max(b0.z, b0.w)),
+                              max(max(b1.x, b1.y), max(b1.z, b1.w)));
+    if (gate_m(wmax) > gate_threshold(tmax, c)) continue;
+    float x[8], y[8];
+    Elem<E>::unpack(a, x);
+    if (rs.resid) Elem<E>::unpack(vd[v], y);
+    const uint32_t w[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int q = 0; q < kPer; ++q)
+      race_offer_td(rs, e + q, x[q], rs.resid ? y[q] : 0.f, w[q], c, bk, bi);
+  }
+  for (int i = nvec * kPer + tid; i < len; i += kConsumers) {  // ragged tail, from global memory
+    const int64_t e = e0 + i;
+    const float t = Elem<E>::load(trow, e);
+    if (!(t >= floor_t)) continue;
+    const float d = rs.resid ? Elem<E>::load(drow, e) : 0.f;
+    const uint4 b = stream_block(rs.st, static_cast<uint32_t>(e >> 2));
+    race_offer_td(rs, e, t, d, word_of(b, static_cast<uint32_t>(e & 3)), c, bk, bi);
+  }
+}
+
+// The race's winner and the request's outputs, by the warp that merged the race; a residual with
+// no positive entry left (p and q agree to working precision) is drawn from p with the same
+// uniforms, by this warp over the whole row.
+template <typename E>
+__device__ void block_finish(const BlockParams& p, const BlockMeta& m, const RaceSpec& rs,
+                             const RaceDesc& d, int32_t y) {
+  const int lane = threadIdx.x & 31;
+  if (y < 0 && rs.resid) {
+    RaceSpec fb = rs;
+    fb.resid = false;
+    float bk = -INFINITY;
+    int32_t bi = -1;
+    for (int64_t e = lane; e < p.V; e += 32) {
+      const float t = Elem<E>::load(m.trow, e);
+      const float k = race_exact_td(fb, e, t, 0.f);
+      if (k > -INFINITY && race_better(k, int32_t(e), bk, bi)) {
+        bk = k;
+        bi = int32_t(e);
+      }
+    }
+    warp_race(bk, bi);
+    y = bi;
+  }
+  int32_t* out = p.out_tokens + size_t(m.r) * p.out_ld;
+  for (int64_t q = lane; q < p.out_ld; q += 32) {
+    int32_t v = -1;
+    if (q < d.tau) v = p.draft_tokens[p.draft_row0[m.r] + q];
+    else if (q == d.tau) v = y;
+    out[q] = v;
+  }
+  if (lane == 0) {
+    if (y < 0) report(p.status, SV_ERR_BAD_INPUT);  // the row carries no probability at all
+    p.accepted_len[m.r] = d.tau;
+    if (p.correction_token) p.correction_token[m.r] = y;
+  }
 }
 
 template <typename E>
@@ -653,6 +823,9 @@ __device__ void block_consumer(const BlockParams& p, const uint8_t* ring, uint64
   float2 gap = splat2(0.f), nmt = splat2(0.f);
   float A = 0.f;
   int32_t cur_seg = -1;
+  RaceSpec rs{};  // the race of the request in flight
+  float bk = -INFINITY;
+  int32_t bi = -1;
   for (uint32_t n = 0;; ++n) {
     const uint32_t stage = n % kRing;
     if (!mbar_wait(&full[stage], (n / kRing) & 1, p.status)) return;
@@ -724,6 +897,34 @@ __device__ void block_consumer(const BlockParams& p, const uint8_t* ring, uint64
           acc = resid_pair(acc, t, d, gap, nmt);
         }
       }
+    } else if (m.kind == kSegRace) {
+      if (m.seg != cur_seg) {
+        // first stage of the request's race: its stream, then a bound from this stage's seeds
+        int32_t ok = 1;
+        if (lane == 0) ok = wait_seq(&bs->desc_seq, m.seq, p.status);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+        __syncwarp();
+        const RaceDesc d = bs->desc;
+        const uint64_t req = p.request_ids ? p.request_ids[m.r] : uint64_t(m.r);
+        rs.resid = d.resid != 0;
+        rs.gap = d.gap;
+        rs.st = make_stream(p.seed, req, uint32_t(d.tau + 1), rs.resid ? kTagResid : kTagBonus);
+        cur_seg = m.seg;
+        int32_t si;
+        const float sk = race_stage_seed<E>(rs, vt, vd, nvec, m.e0, tid, si);
+        bk = sk > -INFINITY ? sk : -INFINITY;
+        bi = sk > -INFINITY ? si : -1;
+        const float wk = warp_max(sk);
+        if (lane == 0 && wk > -INFINITY) atomicMax(&bs->race_k0, key_order(wk));
+        __syncwarp();
+      }
+      // the bound: the best exact key any warp has published (each an entry of this row, so never
+      // above the winner's key); a warp that reads it before the others publish gates more loosely
+      const float K0 = fmaxf(warp_max(bk),
+                             key_from_order(*reinterpret_cast<volatile uint32_t*>(&bs->race_k0)));
+      race_stage_main<E>(rs, vt, vd, nvec, m.len, m.e0, m.trow, m.drow, tid, K0, bk, bi);
+      const float wk = warp_max(bk);
+      if (lane == 0 && wk > K0) atomicMax(&bs->race_k0, key_order(wk));
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
@@ -736,6 +937,10 @@ __device__ void block_consumer(const BlockParams& p, const uint8_t* ring, uint64
       warp_ms2(md, sd);
     } else if (m.kind == kSegResid) {
       st = warp_sum(acc.x + acc.y);
+    } else if (m.kind == kSegRace) {
+      warp_race(bk, bi);
+      mt = bk;
+      st = __int_as_float(bi);
     }
     int32_t last = 0;
     if (lane == 0) {
@@ -791,8 +996,17 @@ __device__ void block_consumer(const BlockParams& p, const uint8_t* ring, uint64
         float a = lane < kConsumerWarps ? bs->dep[buf][lane][1] : 0.f;
         a = warp_sum(a);
         if (lane == 0) bs->R[m.row - 1] = a * A;
+      } else if (m.kind == kSegRace) {
+        float k = -INFINITY;
+        int32_t i = -1;
+        if (lane < kConsumerWarps) {
+          k = bs->dep[buf][lane][0];
+          i = __float_as_int(bs->dep[buf][lane][1]);
+        }
+        warp_race(k, i);
+        block_finish<E>(p, m, rs, bs->desc, i);
       } else {
-        block_decide<E>(p, m.r, bs);
+        block_decide<E>(p, m.r, m.seq, bs);
       }
       __syncwarp();
       if (lane == 0) bs->count[buf] = 0;
@@ -802,6 +1016,8 @@ __device__ void block_consumer(const BlockParams& p, const uint8_t* ring, uint64
     md = kM2Empty;
     sd = 0.f;
     acc = make_float2(0.f, 0.f);
+    bk = -INFINITY;
+    bi = -1;
   }
 }
 
@@ -823,6 +1039,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) block_kernel(BlockParams p)
       bs.rho_seq[k] = 0u;
     }
     bs.bad = 0;
+    bs.desc_seq = 0u;
+    bs.race_k0 = 0u;
     fence_barrier_init();
   }
   // the race kernel that follows may launch now (it waits for this grid's results itself)
@@ -1176,12 +1394,19 @@ static sv_status run_verify(bool block, const CommonArgs& a, const int64_t* targ
     bp.request_ids = request_ids;
     bp.rho_out = ratio_out;
     bp.h_out = h_out;
+    bp.accepted_len = accepted_len;
+    bp.out_tokens = out_tokens;
+    bp.out_ld = out_ld;
+    bp.correction_token = correction_token;
     bp.ws = ws;
     bp.status = status;
     profile_mark(0, stream);
     st = launch_block<E>(bp, stream);
     if (st != SV_OK) return st;
     profile_mark(1, stream);
+    profile_mark(2, stream);
+    profile_mark(3, stream);  // the block kernel draws the correction itself
+    return launch_status(cudaGetLastError());
   }
   profile_mark(2, stream);
 

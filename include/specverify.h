@@ -81,6 +81,14 @@ const char* sv_version(void);
  * sv_profile_read waits for the events of the last profiled call and returns the three durations
  * in milliseconds.  The events belong to the library (created on first use, one set per host
  * thread); nothing is recorded while profiling is disabled. */
+/* Failure-detection self test.  Runs one of the bounded device-side waits the kernels use on a
+ * condition that never comes true -- which = 0: an mbarrier phase no thread completes; which = 1:
+ * a shared-memory request-number word no thread publishes -- with a limit of `limit_us`
+ * microseconds (1 .. 1000000) instead of the kernels' one second.  The wait gives up, writes
+ * SV_ERR_TIMEOUT to the DEVICE word `status` (required; reset first) and the kernel returns, so the
+ * context stays usable.  No page has a counterpart: it checks the library's own safety net. */
+sv_status sv_selftest_wait(int32_t which, int32_t limit_us, int32_t* status, void* stream);
+
 sv_status sv_profile_enable(int enable);
 sv_status sv_profile_read(float* ms_out /* HOST [3] */);
 

@@ -58,6 +58,7 @@ def lib():
             "sv_status_string": (C.c_char_p, [st]),
             "sv_version": (C.c_char_p, []),
             "sv_profile_enable": (st, [C.c_int]),
+            "sv_selftest_wait": (st, [i32, i32, P, P]),
             "sv_profile_read": (st, [P]),
             "spec_verify_workspace_bytes": (sz, [i32, i32, i64, st]),
             "spec_verify_token": (st, verify_args + [P, P, P, sz, P]),
@@ -89,6 +90,12 @@ def status_string(code):
 
 def version():
     return lib().sv_version().decode()
+
+
+def sv_selftest_wait(which, limit_us, status, stream=None):
+    """Make one of the kernels' bounded waits run out (see include/specverify.h)."""
+    _check(lib().sv_selftest_wait(int(which), int(limit_us), _ptr(status), _stream(stream)),
+           "sv_selftest_wait")
 
 
 def sv_profile_enable(enable=True):

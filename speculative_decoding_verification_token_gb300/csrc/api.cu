@@ -1,6 +1,7 @@
 // api.cu -- status strings, version and the host-side device queries used by every entry point.
 #include <mutex>
 
+#include "sv_device.cuh"
 #include "sv_host.h"
 
 namespace sv {
@@ -94,3 +95,37 @@ extern "C" const char* sv_status_string(sv_status status) {
 }
 
 extern "C" const char* sv_version(void) { return "specverify 0.1 (sm_103a)"; }
+
+// ---------------------------------------------------------------------------------------------
+// sv_selftest_wait: the bounded waits of the kernels, made to run out
+// ---------------------------------------------------------------------------------------------
+namespace sv {
+
+// One warp.  which = 0: an mbarrier phase that no thread completes; which = 1: a shared-memory
+// request-number word that no thread publishes.  Both use the waits every kernel uses, with the
+// caller's limit, and must end with SV_ERR_TIMEOUT in `status`.
+__global__ void selftest_wait_kernel(int32_t which, uint64_t limit_ns, int32_t* status) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t word;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    word = 0u;
+  }
+  __syncwarp();
+  if (threadIdx.x != 0) return;
+  if (which == 0) mbar_wait(&bar, 0, status, limit_ns);
+  else wait_seq(&word, 1u, status, limit_ns);
+}
+
+}  // namespace sv
+
+extern "C" sv_status sv_selftest_wait(int32_t which, int32_t limit_us, int32_t* status,
+                                      void* stream) {
+  if ((which != 0 && which != 1) || limit_us <= 0 || limit_us > 1000000 || !status)
+    return SV_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return SV_ERR_CUDA;
+  sv::selftest_wait_kernel<<<1, 32, 0, s>>>(which, uint64_t(limit_us) * 1000ull, status);
+  return sv::launch_status(cudaGetLastError());
+}

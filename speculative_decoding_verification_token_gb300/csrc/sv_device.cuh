@@ -142,17 +142,49 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for phase `parity` of `bar` for at most ~1 s; on expiry report SV_ERR_TIMEOUT and give up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+// Every device-side wait gives up after this long, reports SV_ERR_TIMEOUT and lets its kernel wind
+// down, so that a wait that can never end leaves the GPU usable.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Wait for phase `parity` of `bar` for at most `limit_ns`; on expiry report SV_ERR_TIMEOUT and give
+// up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > 1000000000ull) {
+    if (global_ns() - t0 > limit_ns) {
       report(status, SV_ERR_TIMEOUT);
       return false;
     }
   }
   return true;
+}
+
+// Wait until the request number in shared-memory word `w` reaches `seq`, for at most `limit_ns`;
+// on expiry report SV_ERR_TIMEOUT and give up.
+__device__ __forceinline__ bool wait_seq(const uint32_t* w, uint32_t seq, int32_t* status,
+                                         uint64_t limit_ns = kWaitLimitNs) {
+  const volatile uint32_t* v = w;
+  if (int32_t(*v - seq) >= 0) {
+    __threadfence_block();
+    return true;
+  }
+  const uint64_t t0 = global_ns();
+  while (int32_t(*v - seq) < 0) {
+    if (global_ns() - t0 > limit_ns) {
+      report(status, SV_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  __threadfence_block();
+  return true;
+}
+
+__device__ __forceinline__ void publish_seq(uint32_t* w, uint32_t seq) {
+  __threadfence_block();
+  *reinterpret_cast<volatile uint32_t*>(w) = seq;
 }
 
 // ---- element access ---------------------------------------------------------------------------

@@ -477,30 +477,6 @@ struct BlockState {  // the request in flight, in shared memory
   uint32_t race_k0;              // key_order of the best exact key of the race so far (0: none)
 };
 
-// Wait until the request number in `w` reaches `seq` (bounded; SV_ERR_TIMEOUT on expiry).
-__device__ __forceinline__ bool wait_seq(const uint32_t* w, uint32_t seq, int32_t* status) {
-  const volatile uint32_t* v = w;
-  if (int32_t(*v - seq) >= 0) {
-    __threadfence_block();
-    return true;
-  }
-  const uint64_t t0 = global_ns();
-  while (int32_t(*v - seq) < 0) {
-    if (global_ns() - t0 > 1000000000ull) {
-      report(status, SV_ERR_TIMEOUT);
-      return false;
-    }
-    __nanosleep(64);
-  }
-  __threadfence_block();
-  return true;
-}
-
-__device__ __forceinline__ void publish_seq(uint32_t* w, uint32_t seq) {
-  __threadfence_block();
-  *reinterpret_cast<volatile uint32_t*>(w) = seq;
-}
-
 template <typename E>
 __device__ void block_producer(const BlockParams& p, uint8_t* ring, uint64_t* full,
                                uint64_t* empty, BlockMeta* meta, BlockState* bs) {

@@ -264,6 +264,7 @@ def markov_draft_request(backbone, U, W, anchor, scores, T, seed, req, forced_pr
 
 STOP_FIRST_DROP = 0
 STOP_ARGMAX = 1
+STOP_FIXED_DEPTH = 2
 
 
 def schedule(cond_accept, max_len, sps, B_max, rule=STOP_FIRST_DROP):

@@ -527,7 +527,8 @@ int orc_schedule_rule(const float* cond_accept, const int32_t* max_len, int32_t 
                       const double* sps, int32_t B_max, int32_t rule, int32_t* sel_len,
                       float* survival, int32_t* total_rows, double* objective) {
   if (N < 0 || K < 0 || B_max < N || !sel_len || !total_rows || !objective) return ORC_ERR_ARGS;
-  if (rule != ORC_STOP_FIRST_DROP && rule != ORC_STOP_ARGMAX) return ORC_ERR_ARGS;
+  if (rule != ORC_STOP_FIRST_DROP && rule != ORC_STOP_ARGMAX && rule != ORC_STOP_FIXED_DEPTH)
+    return ORC_ERR_ARGS;
   int64_t n_items = 0;
   for (int32_t i = 0; i < N; ++i) {
     if (max_len[i] < 0 || max_len[i] > K) return ORC_ERR_ARGS;
@@ -554,9 +555,39 @@ int orc_schedule_rule(const float* cond_accept, const int32_t* max_len, int32_t 
     }
     sel_len[i] = 0;
   }
+  const double two40 = ldexp(1.0, 40);
+  if (rule == ORC_STOP_FIXED_DEPTH) {
+    /* one depth k for every request (min(k, max_len) drafts each): T(k) = N + sum of survivals up
+       to depth k, B(k) = N + sum of min(k, max_len); stop at the first k whose next depth does not
+       raise f, or whose next depth would exceed B_max */
+    int64_t Tk = (int64_t)N << 40, Bk = N;
+    double f = (double)Tk * ldexp(1.0, -40) * sps[N];
+    int32_t depth = 0;
+    for (int32_t k = 1; k <= K; ++k) {
+      int64_t Tn = Tk, Bn = Bk;
+      for (int32_t i = 0; i < N; ++i) {
+        if (k > max_len[i]) continue;
+        float S = 1.0f;
+        for (int32_t j = 1; j <= k; ++j) S = S * cond_accept[(int64_t)i * K + (j - 1)];
+        Tn += (int64_t)floor((double)S * two40);
+        Bn += 1;
+      }
+      if (Bn > (int64_t)B_max || Bn == Bk) break;
+      double fn = (double)Tn * ldexp(1.0, -40) * sps[Bn];
+      if (!(fn > f)) break;
+      Tk = Tn;
+      Bk = Bn;
+      f = fn;
+      depth = k;
+    }
+    for (int32_t i = 0; i < N; ++i) sel_len[i] = depth < max_len[i] ? depth : max_len[i];
+    *total_rows = (int32_t)Bk;
+    *objective = f;
+    free(items);
+    return ORC_OK;
+  }
   qsort(items, (size_t)n_items, sizeof(sched_item), item_order);
 
-  const double two40 = ldexp(1.0, 40);
   int64_t Tb = (int64_t)N << 40; /* one guaranteed token per request, in 2^-40 units */
   double f = (double)Tb * ldexp(1.0, -40) * sps[N];
   int64_t b = 0;

@@ -195,7 +195,15 @@ int orc_schedule(const float* cond_accept, const int32_t* max_len, int32_t N, in
  * in [TC] "Adaptive verification" (each budget filled with the positions most likely to survive,
  * the best one kept): b* = the smallest b in 0..min(items, B_max - N) with f(b) = max f.  The order,
  * F, T and f are the same as above. */
-enum { ORC_STOP_FIRST_DROP = 0, ORC_STOP_ARGMAX = 1 };
+enum { ORC_STOP_FIRST_DROP = 0, ORC_STOP_ARGMAX = 1, ORC_STOP_FIXED_DEPTH = 2 };
+/* FIXED_DEPTH: the fixed-depth cost model of [TC] "Our own simple cost model" -- every request
+ * verifies the same number k of drafts (min(k, max_len[i])), and one more slot is worth adding only
+ * while it raises the expected tokens per unit time: with L_k = expected tokens (the guaranteed one
+ * plus the survivals up to depth k) and C_k = the step time at the rows of depth k, slot k + 1 pays
+ * when its survival exceeds L_k (C_{k+1} - C_k) / C_k, i.e. when f(k + 1) > f(k) with
+ * f(k) = T(k) 2^-40 sps[B(k)], T(k) = N 2^40 + sum of F up to depth k, B(k) = N + sum of
+ * min(k, max_len).  The depth is the first k where the next one does not pay (or would exceed
+ * B_max); sel_len[i] = min(k, max_len[i]). */
 int orc_schedule_rule(const float* cond_accept, const int32_t* max_len, int32_t N, int32_t K,
                       const double* sps, int32_t B_max, int32_t rule, int32_t* sel_len,
                       float* survival, int32_t* total_rows, double* objective);

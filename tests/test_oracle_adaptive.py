@@ -240,3 +240,76 @@ def test_sts_preserves_the_order_of_confidences(orc):
         order = np.argsort(s[:, k], kind="stable")
         c = 1.0 / (1.0 + np.exp(-s[order, k].astype(np.float64) / float(T[k])))
         assert np.all(np.diff(c) >= 0.0)
+
+
+# ---- fixed-depth cost model ---------------------------------------------------------------------
+
+def test_fixed_depth_hand_worked(orc):
+    """Two requests, c = (0.9, 0.5) and (0.5, 0.9): survivals (0.9, 0.45) and (0.5, 0.45).
+    Depth 0, 1, 2: expected tokens L = 2, 3.4, 4.3 on B = 2, 4, 6 rows.  With step time
+    C(B) = 1 + 0.1 B the throughput L / C is 1.67, 2.43, 2.69: depth 2.  With C(B) = 1 + 0.3 B it is
+    1.25, 1.545, 1.536: slot 2 adds 0.9 expected tokens but would need 3.4 * (2.8 - 2.2) / 2.2 =
+    0.93, so depth 1."""
+    c = np.array([[0.9, 0.5], [0.5, 0.9]], np.float32)
+    B = np.arange(7)
+    r = orc.schedule(c, [2, 2], 1.0 / (1.0 + 0.1 * B), 6, rule=orc.STOP_FIXED_DEPTH)
+    assert r["status"] == 0 and r["total_rows"] == 6 and list(r["sel_len"]) == [2, 2]
+    assert abs(r["objective"] - 4.3 / 1.6) < 1e-6
+    r = orc.schedule(c, [2, 2], 1.0 / (1.0 + 0.3 * B), 6, rule=orc.STOP_FIXED_DEPTH)
+    assert r["total_rows"] == 4 and list(r["sel_len"]) == [1, 1]
+    assert abs(r["objective"] - 3.4 / 2.2) < 1e-6
+
+
+def _marginal_depth(c, max_len, sps, B_max):
+    """The page's marginal rule in exact rational arithmetic: slot k + 1 pays while its survival
+    mass p exceeds L_k (C_{k+1} - C_k) / C_k, with C = 1 / SPS."""
+    from fractions import Fraction
+    N, K = c.shape
+    S = np.ones(N, np.float32)
+    surv = []
+    for k in range(1, K + 1):
+        S = np.where(max_len >= k, (S * c[:, k - 1]).astype(np.float32), np.float32(0))
+        surv.append([int(np.floor(float(s) * 2.0 ** 40)) if max_len[i] >= k else None
+                     for i, s in enumerate(S)])
+    L, B, depth = Fraction(N), N, 0
+    for k in range(1, K + 1):
+        add = [f for f in surv[k - 1] if f is not None]
+        Bn = B + len(add)
+        if Bn > B_max or Bn == B:
+            break
+        p = Fraction(sum(add), 2 ** 40)
+        Ck, Cn = 1 / Fraction(sps[B]), 1 / Fraction(sps[Bn])
+        if not p > L * (Cn - Ck) / Ck:
+            break
+        L, B, depth = L + p, Bn, k
+    return depth, B
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_fixed_depth_is_the_marginal_rule(orc, seed):
+    rng = np.random.default_rng(1300 + seed)
+    N, K = int(rng.integers(1, 30)), int(rng.integers(1, 10))
+    c = (rng.beta(8, 2, (N, K)) * 0.95 ** np.arange(K)).astype(np.float32)
+    max_len = rng.integers(0, K + 1, N).astype(np.int32)
+    B_max = int(N + rng.integers(0, N * K + 2))
+    sps = 1.0 / (2e-3 + np.arange(B_max + 1) * rng.uniform(1e-5, 3e-4))
+    depth, rows = _marginal_depth(c, max_len, sps, B_max)
+    r = orc.schedule(c, max_len, sps, B_max, rule=orc.STOP_FIXED_DEPTH)
+    assert r["status"] == 0
+    assert r["total_rows"] == rows
+    assert (r["sel_len"] == np.minimum(depth, max_len)).all()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_best_budget_dominates_fixed_depth(orc, seed):
+    """For any row count the sorted prefix holds the largest survivals, so the best budget over
+    sorted prefixes is never below the fixed-depth choice."""
+    rng = np.random.default_rng(1400 + seed)
+    N, K = 50, 8
+    c = (rng.beta(8, 2, (N, K)) * 0.97 ** np.arange(K)).astype(np.float32)
+    max_len = rng.integers(0, K + 1, N).astype(np.int32)
+    B_max = N * (K + 1)
+    sps = 1.0 / (2e-3 + np.arange(B_max + 1) * 2e-5)
+    best = orc.schedule(c, max_len, sps, B_max, rule=orc.STOP_ARGMAX)
+    fixed = orc.schedule(c, max_len, sps, B_max, rule=orc.STOP_FIXED_DEPTH)
+    assert best["objective"] >= fixed["objective"]

@@ -374,6 +374,15 @@ def bench_rows(steps, warmup):
     rows["schedule_best_budget_512x16"] = {
         "us": sum(t) / len(t) * 1e6, "total_rows": int(sched["o"]["total_rows"].item()),
         "status": int(status.item())}
+
+    def sch_depth():
+        sched["o"] = sv.dspark_schedule(c, ml, sps, si["B_max"], status=status, workspace=sws,
+                                        rule=sv.SV_STOP_FIXED_DEPTH)
+    t = time_calls(sch_depth, steps, warmup, flush, stream)
+    rows["schedule_fixed_depth_512x16"] = {
+        "us": sum(t) / len(t) * 1e6, "total_rows": int(sched["o"]["total_rows"].item()),
+        "status": int(status.item())}
+    sch_best()  # the acceptance update below reads the best-budget selection
     sel = sched["o"]["sel_len"]
     acc = torch.minimum(sel, torch.arange(sw.N, device=dev, dtype=torch.int32) % 5)
     trials = torch.zeros(sw.K, dtype=torch.float64, device=dev)

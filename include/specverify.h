@@ -244,8 +244,13 @@ sv_status dspark_schedule(const float* cond_accept, const int32_t* max_len, int3
  *   SV_STOP_ARGMAX      the budget with the highest expected tokens per unit time over every
  *                       admissible budget b = 0 .. min(items, B_max - N), the smallest b among
  *                       equals (vLLM's choice in "How much does a token cost", "Adaptive
- *                       verification"). */
-typedef enum { SV_STOP_FIRST_DROP = 0, SV_STOP_ARGMAX = 1 } sv_stop_rule;
+ *                       verification").
+ *   SV_STOP_FIXED_DEPTH one depth k for every request (min(k, max_len) drafts each), deepened while
+ *                       the next depth still raises f -- the marginal-slot condition of "How much
+ *                       does a token cost", "Our own simple cost model" (slot k + 1 pays when its
+ *                       survival mass exceeds L_k (C_{k+1} - C_k) / C_k, C the step time) -- and
+ *                       stays within B_max.  total_rows and objective are those of that depth. */
+typedef enum { SV_STOP_FIRST_DROP = 0, SV_STOP_ARGMAX = 1, SV_STOP_FIXED_DEPTH = 2 } sv_stop_rule;
 
 /* dspark_schedule with a choice of stopping rule (`rule`, an sv_stop_rule); the order, the fixed
  * point sums and f(b) are those of dspark_schedule, and so are the arguments, outputs, errors and

@@ -305,12 +305,14 @@ def dspark_schedule_workspace_bytes(N, K):
 
 SV_STOP_FIRST_DROP = 0
 SV_STOP_ARGMAX = 1
+SV_STOP_FIXED_DEPTH = 2
 
 
 def dspark_schedule(cond_accept, max_len, sps, B_max, want_survival=True, status=None,
                     workspace=None, stream=None, rule=SV_STOP_FIRST_DROP):
     """Hardware-aware prefix scheduler.  cond_accept fp32 [N, K]; sps fp64 [B_max + 1]; rule:
-    SV_STOP_FIRST_DROP (early stop) or SV_STOP_ARGMAX (best budget over all)."""
+    SV_STOP_FIRST_DROP (early stop), SV_STOP_ARGMAX (best budget over all) or
+    SV_STOP_FIXED_DEPTH (one depth for every request)."""
     _dev(cond_accept, torch.float32), _dev(max_len, torch.int32), _dev(sps, torch.float64)
     N, K = cond_accept.shape
     dev = cond_accept.device

@@ -52,6 +52,8 @@ struct ScheduleParams {
   uint64_t* chunk_keys;   // workspace [n_chunks][CL]: each chunk's keys, sorted
   long long* sorted_F;    // workspace [N * K]: F of the prefix of rank b, at b
   int32_t* sorted_req;    // workspace [N * K]: the request of the prefix of rank b, at b
+  unsigned long long* depth_F;  // workspace [K] (fixed-depth rule): sum of F at depth k + 1
+  unsigned long long* depth_n;  // workspace [K] (fixed-depth rule): requests reaching depth k + 1
 };
 
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -149,6 +151,10 @@ __global__ void __launch_bounds__(kChunkThreads) schedule_chunk_kernel(ScheduleP
         }
         run[k - 1] = key;
         if (p.survival) p.survival[size_t(i) * p.K + (k - 1)] = out;
+        if (p.rule == SV_STOP_FIXED_DEPTH && k <= L) {  // exact integer sums per depth
+          atomicAdd(&p.depth_F[k - 1], static_cast<unsigned long long>(fixed40(key)));
+          atomicAdd(&p.depth_n[k - 1], 1ull);
+        }
       }
     }
   }
@@ -420,6 +426,36 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_admit_kernel(ScheduleP
   for (int32_t i = tid; i < p.N; i += kSchedThreads) p.sel_len[i] = counts[i];
 }
 
+// The fixed-depth rule, one CTA: one depth k for every request (min(k, max_len) drafts each),
+// deepened while f(k + 1) = T(k + 1) 2^-40 sps[B(k + 1)] exceeds f(k) and B(k + 1) <= B_max, from
+// the chunk kernel's exact per-depth sums of F and request counts.
+__global__ void __launch_bounds__(kSchedThreads) schedule_depth_kernel(ScheduleParams p) {
+  __shared__ int32_t s_depth;
+  const int tid = threadIdx.x;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the chunk kernel's sums
+  if (tid == 0) {
+    long long T = static_cast<long long>(p.N) << 40, B = p.N;
+    double f = static_cast<double>(T) * kTwoM40 * p.sps[p.N];
+    int32_t depth = 0;
+    for (int32_t k = 1; k <= p.K; ++k) {
+      const long long Tn = T + static_cast<long long>(__ldcg(p.depth_F + (k - 1)));
+      const long long Bn = B + static_cast<long long>(__ldcg(p.depth_n + (k - 1)));
+      if (Bn > p.B_max || Bn == B) break;
+      const double fn = static_cast<double>(Tn) * kTwoM40 * p.sps[Bn];
+      if (!(fn > f)) break;
+      T = Tn;
+      B = Bn;
+      f = fn;
+      depth = k;
+    }
+    *p.total_rows = static_cast<int32_t>(B);
+    *p.objective = f;
+    s_depth = depth;
+  }
+  __syncthreads();
+  for (int32_t i = tid; i < p.N; i += kSchedThreads) p.sel_len[i] = min(s_depth, clamp_len(p, i));
+}
+
 // Launches `kernel` as a programmatic dependent of the previous kernel on `stream`.
 template <typename... Args>
 static cudaError_t launch_dependent(void (*kernel)(Args...), unsigned grid, int threads,
@@ -456,7 +492,8 @@ static size_t schedule_ws_bytes(int32_t N, int32_t K) {
   const ChunkShape c = chunk_shape(N, K);
   const size_t nk = size_t(std::max<int64_t>(int64_t(N) * K, 1));
   return align256(sizeof(uint64_t) * size_t(c.n_chunks) * size_t(c.CL)) +
-         align256(sizeof(long long) * nk) + align256(sizeof(int32_t) * nk);
+         align256(sizeof(long long) * nk) + align256(sizeof(int32_t) * nk) +
+         align256(2 * sizeof(unsigned long long) * size_t(std::max(K, 1)));
 }
 
 }  // namespace sv
@@ -473,7 +510,8 @@ extern "C" sv_status dspark_schedule_rule(const float* cond_accept, const int32_
                                           int32_t rule, int32_t* sel_len, float* survival,
                                           int32_t* total_rows, double* objective, int32_t* status,
                                           void* workspace, size_t workspace_bytes, void* stream) {
-  if (rule != SV_STOP_FIRST_DROP && rule != SV_STOP_ARGMAX) return SV_ERR_INVALID;
+  if (rule != SV_STOP_FIRST_DROP && rule != SV_STOP_ARGMAX && rule != SV_STOP_FIXED_DEPTH)
+    return SV_ERR_INVALID;
   if (N < 0 || K < 0 || B_max < N) return SV_ERR_INVALID;
   if (!sel_len || !total_rows || !objective || !sps) return SV_ERR_INVALID;
   if (N > 0 && K > 0 && !cond_accept) return SV_ERR_INVALID;
@@ -504,12 +542,19 @@ extern "C" sv_status dspark_schedule_rule(const float* cond_accept, const int32_
   p.chunk_keys = reinterpret_cast<uint64_t*>(ws);
   p.sorted_F = reinterpret_cast<long long*>(ws + keys_bytes);
   p.sorted_req = reinterpret_cast<int32_t*>(ws + keys_bytes + f_bytes);
+  p.depth_F = reinterpret_cast<unsigned long long*>(
+      ws + keys_bytes + f_bytes + align256(sizeof(int32_t) * size_t(NK > 0 ? NK : 1)));
+  p.depth_n = p.depth_F + std::max(K, 1);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (status && cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return SV_ERR_CUDA;
   const int sms = device_sm_count();
   const int smem_sm = device_smem_per_sm();
   if (sms <= 0 || smem_sm <= 0) return SV_ERR_CUDA;
 
+  if (rule == SV_STOP_FIXED_DEPTH &&
+      cudaMemsetAsync(p.depth_F, 0, 2 * sizeof(unsigned long long) * size_t(std::max(K, 1)), s) !=
+          cudaSuccess)
+    return SV_ERR_CUDA;
   profile_mark(0, s);
   // chunk: one CTA per chunk of R requests; double-buffered keys
   const size_t chunk_smem = 2 * sizeof(uint64_t) * size_t(cs.CL);
@@ -519,6 +564,13 @@ extern "C" sv_status dspark_schedule_rule(const float* cond_accept, const int32_
   if (e != cudaSuccess) return SV_ERR_CUDA;
   schedule_chunk_kernel<<<unsigned(cs.n_chunks), kChunkThreads, chunk_smem, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  if (rule == SV_STOP_FIXED_DEPTH) {  // no ranking: the depth kernel reads the per-depth sums
+    profile_mark(1, s);
+    profile_mark(2, s);
+    e = launch_dependent(schedule_depth_kernel, 1, kSchedThreads, 0, s, p);
+    profile_mark(3, s);
+    return launch_status(e);
+  }
   // rank: every SM (as many CTAs as fit), each staging all chunks
   const size_t rank_smem = sizeof(uint64_t) * size_t(cs.n_chunks) * size_t(cs.CL);
   const int per_sm = std::max(1, std::min(4, smem_sm / int(rank_smem + 2048)));

@@ -117,10 +117,11 @@ def _gpu_schedule_rule(sv, c, max_len, sps, B_max, rule):
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
+@pytest.mark.parametrize("rule", ["argmax", "fixed_depth"])
 @pytest.mark.parametrize("seed", range(6))
-def test_schedule_argmax_rule_matches_oracle(sv, orc, seed):
-    """Best budget over all budgets, bit-exact, on random tables with a bumpy SPS curve (several
-    local maxima of f) and ties."""
+def test_schedule_argmax_rule_matches_oracle(sv, orc, seed, rule):
+    """Best budget over all budgets, and one depth for every request, bit-exact, on random tables
+    with a bumpy SPS curve (several local maxima of f) and ties."""
     rng = np.random.default_rng(900 + seed)
     N = int(rng.integers(1, 700))
     K = int(rng.integers(1, 20))
@@ -134,9 +135,11 @@ def test_schedule_argmax_rule_matches_oracle(sv, orc, seed):
     B_max = int(N + rng.integers(0, 3 * N * K // 4 + 2))
     b = np.arange(B_max + 1)
     sps = 1.0 / (2e-3 + b * rng.uniform(1e-8, 1e-4)) * (1.0 + 0.05 * np.sin(0.3 * b))
-    ref = orc.schedule(c, max_len, sps, B_max, rule=orc.STOP_ARGMAX)
+    o_rule, g_rule = ((orc.STOP_ARGMAX, sv.SV_STOP_ARGMAX) if rule == "argmax"
+                      else (orc.STOP_FIXED_DEPTH, sv.SV_STOP_FIXED_DEPTH))
+    ref = orc.schedule(c, max_len, sps, B_max, rule=o_rule)
     assert ref["status"] == 0
-    got = _gpu_schedule_rule(sv, c, max_len, sps, B_max, sv.SV_STOP_ARGMAX)
+    got = _gpu_schedule_rule(sv, c, max_len, sps, B_max, g_rule)
     assert (got["sel_len"] == ref["sel_len"]).all()
     assert int(got["total_rows"][0]) == ref["total_rows"]
     assert got["objective"][0] == ref["objective"]
@@ -144,7 +147,7 @@ def test_schedule_argmax_rule_matches_oracle(sv, orc, seed):
 
 def test_schedule_argmax_rule_workload_and_edges(sv, orc):
     inp = synth.schedule_inputs(synth.SCHEDULE)
-    for rule in (sv.SV_STOP_ARGMAX, sv.SV_STOP_FIRST_DROP):
+    for rule in (sv.SV_STOP_ARGMAX, sv.SV_STOP_FIRST_DROP, sv.SV_STOP_FIXED_DEPTH):
         ref = orc.schedule(inp["cond_accept"], inp["max_len"], inp["sps"], inp["B_max"],
                            rule=rule)
         got = _gpu_schedule_rule(sv, inp["cond_accept"], inp["max_len"], inp["sps"],

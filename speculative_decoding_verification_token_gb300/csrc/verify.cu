@@ -1215,16 +1215,15 @@ struct CommonArgs {
 };
 
 // CTAs per race job for rows of S 16 KB slices: each owns one contiguous share of the row.
-// When the jobs times kRaceSplitMax shares fit in one wave of resident race CTAs, the shares are
-// made as many as still fit (up to kRaceSplitFew), so that no SM holds more work than it must;
-// otherwise kRaceSplitMax shares per job.
+// Shares per job: as many as one wave of resident race CTAs holds (up to kRaceSplitFew), so that
+// every job's shares run at once and no CTA pays the decide, seed and combine latencies twice; at
+// least one share per job (then several waves).
 static int32_t race_split(int32_t S, int64_t jobs) {
   int32_t cl = kRaceSplitMax;
   const int sms = device_sm_count();
   if (sms > 0 && jobs > 0) {
     const int64_t slots = int64_t(sms) * kRaceCtasPerSm;
-    if (jobs * kRaceSplitMax <= slots)
-      cl = int32_t(std::min<int64_t>(kRaceSplitFew, slots / jobs));
+    cl = int32_t(std::max<int64_t>(1, std::min<int64_t>(kRaceSplitFew, slots / jobs)));
   }
   return std::max(1, std::min(cl, S));
 }

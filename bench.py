@@ -426,6 +426,15 @@ def bench_rows(steps, warmup):
                                         status=status, workspace=ws2)
         rnd["s"] = s
     t = time_calls(round_, steps, warmup, flush, stream)
+    # the verify call's kernels (stream, race), from the library's events (the last call records)
+    sv.sv_profile_enable(True)
+    parts = []
+    for _ in range(max(3, steps // 2)):
+        flush()
+        round_()
+        parts.append(sv.sv_profile_read())
+    sv.sv_profile_enable(False)
+    vkms = [sum(q[k] for q in parts) / len(parts) for k in range(3)]
     sel = rnd["s"]["sel_len"].cpu()
     acc = rnd["o"]["accepted_len"].cpu()
     n_bonus = int((acc == sel).sum())
@@ -433,7 +442,9 @@ def bench_rows(steps, warmup):
     tm = sum(t) / len(t)
     rows["scheduled_round_512x16_V129280_bf16"] = {
         "ms": tm * 1e3, "GB_s": nb / tm / 1e9, "positions_per_s": int(sel.sum()) / tm,
-        "verified_rows": int(rnd["s"]["total_rows"].item()), "status": int(status.item())}
+        "verified_rows": int(rnd["s"]["total_rows"].item()),
+        "verify_kernel_ms": {"stream": round(vkms[0], 4), "race_with_decide": round(vkms[2], 4)},
+        "status": int(status.item())}
     del vin, vt
 
     rows["markov_draft_256x16_V151936_R256"] = bench_markov(steps, warmup, flush, stream)

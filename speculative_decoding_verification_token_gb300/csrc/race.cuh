@@ -123,8 +123,9 @@ __device__ __forceinline__ float gate_m(uint32_t w) {
   return static_cast<float>(0x7FFFFFu - (w >> 9));  // exact: below 2^23
 }
 
-constexpr int kSeedBatch = 4;  // vectors whose loads each thread issues before using any (seed)
-constexpr int kBatch = 2;      // the same for the main pass
+constexpr int kSeedBatch = 8;  // vectors whose loads each thread issues before using any (seed)
+constexpr int kBatch = 2;      // the same for the main pass over a staged share
+constexpr int kBatchGlobal = 4;  // ... and over a share read from global memory
 
 // Seed pass over vocabulary range [e0, e0 + len): the exact key of this thread's entry of largest
 // logit (-inf if that entry carries no weight) -- a lower bound on the range's winning key.
@@ -187,7 +188,7 @@ __device__ __forceinline__ void offer(const RaceSpec& rs, const uint8_t* trow,
 
 // Main pass over [e0, e0 + len) against the lower bound K0: only the target row is read; the
 // draft row is touched for the few entries keyed exactly.
-template <typename E>
+template <typename E, int NB = kBatch>
 __device__ __forceinline__ void race_range(const RaceSpec& rs, const uint4* vsrc,
                                            const uint8_t* trow, const uint8_t* drow, int64_t e0,
                                            int32_t len, float K0, float& bk, int32_t& bi) {
@@ -195,15 +196,15 @@ __device__ __forceinline__ void race_range(const RaceSpec& rs, const uint4* vsrc
   const float floor_t = K0 - kMaxNoise;  // no noise lifts a logit below this to K0
   const float c = 23.0f - K0 * kLog2e;
   const int nvec = len / kPer;
-  for (int v0 = threadIdx.x; v0 < nvec; v0 += kThreads * kBatch) {
-    uint4 a[kBatch];
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += kThreads * NB) {
+    uint4 a[NB];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
+    for (int u = 0; u < NB; ++u) {
       const int v = v0 + u * kThreads;
       if (v < nvec) a[u] = vsrc[v];
     }
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
+    for (int u = 0; u < NB; ++u) {
       const int v = v0 + u * kThreads;
       if (v >= nvec) break;
       const int64_t e = e0 + int64_t(v) * kPer;

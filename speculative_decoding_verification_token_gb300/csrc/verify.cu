@@ -1151,7 +1151,10 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) race_kernel(RacePara
   // main pass: only entries whose logit and noise can reach K0 are keyed
   float bk = -INFINITY;
   int32_t bi = -1;
-  if (active) race_range<E>(rs, vsrc, trow, drow, lo, int32_t(hi - lo), K0, bk, bi);
+  if (active) {
+    if (staged) race_range<E>(rs, vsrc, trow, drow, lo, int32_t(hi - lo), K0, bk, bi);
+    else race_range<E, kBatchGlobal>(rs, vsrc, trow, drow, lo, int32_t(hi - lo), K0, bk, bi);
+  }
   block_race(bk, bi, red_k, red_i);
 
   // combine the shares: a 64-bit max over (order-preserving key bits, ~index), so equal keys go

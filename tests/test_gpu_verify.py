@@ -140,6 +140,20 @@ def test_block_without_row_outputs(sv, orc, case):
     assert torch.equal(gpu["out_tokens"], full["out_tokens"])
 
 
+@pytest.mark.parametrize("block", [0, 1])
+def test_more_requests_than_sms(sv, orc, block):
+    """400 requests with ragged lengths: the block kernel's CTAs each walk several requests in
+    turn (request numbers, the shared race bound and the decision reused), with and without the
+    per-row outputs."""
+    w = synth.scaled(synth.BLOCK_LARGE, B=400, V=3000)
+    inp = _to_dev(synth.token_inputs(w, device="cpu",
+                                     draft_len=synth.ragged_lengths(400, 7, seed=13)))
+    tokens = oracle_tokens(orc, inp)
+    _parity(sv, orc, block, inp, tokens=tokens)
+    if block:
+        _parity(sv, orc, block, inp, tokens=tokens, want_rows=False)
+
+
 def test_sampler_matches_oracle(sv, orc):
     """Draft tokens raced from q on the GPU equal the oracle's, except counted near-ties."""
     for w in (synth.TOKEN_SMALL, synth.scaled(synth.TOKEN_LARGE, B=16, V=50000)):

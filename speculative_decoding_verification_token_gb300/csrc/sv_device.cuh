@@ -74,6 +74,17 @@ __device__ __forceinline__ float uniform_of(uint32_t w) {
 // have u close to 1, where E must keep its relative precision.
 __device__ __forceinline__ float race_noise(float u) { return -logf(-logf(u)); }
 
+// ---- ordering atomics ------------------------------------------------------------------------
+// Add with acquire-release semantics at GPU scope: this thread's earlier writes are ordered before
+// the add, and writes ordered before earlier adds on the same word are visible after it -- the
+// ordering a "last one to arrive" count needs, without a sequentially consistent fence.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 // ---- status word ---------------------------------------------------------------------------
 __device__ __forceinline__ void report(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);

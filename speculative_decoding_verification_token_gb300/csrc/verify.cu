@@ -1161,13 +1161,12 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) race_kernel(RacePara
   // to the lower index; the last share to arrive writes the job's outputs
   if (tid == 0) {
     if (bi >= 0) atomicMax(&slot->best, race_pack(bk, bi));
-    __threadfence();
-    s_last = atomicAdd(&slot->count, 1u) == uint32_t(p.CL - 1);
+    // release: this share's maximum before its count; acquire (last share): every share's
+    s_last = atom_add_acq_rel(&slot->count, 1u) == uint32_t(p.CL - 1);
   }
   __syncthreads();
   if (!s_last || !active) return;
   if (tid == 0) {
-    __threadfence();
     const unsigned long long best = atomicAdd(&slot->best, 0ull);
     s_winner = best ? race_unpack_index(best) : -1;
   }

@@ -154,6 +154,20 @@ def test_more_requests_than_sms(sv, orc, block):
         _parity(sv, orc, block, inp, tokens=tokens, want_rows=False)
 
 
+@pytest.mark.parametrize("gamma,noise", [(32, 0.02), (32, 1.0), (40, 0.02)])
+def test_long_drafts(sv, orc, gamma, noise):
+    """Token-level verification of long drafts (32 and 40 positions).  A small draft perturbation
+    makes long accepted runs and bonus tokens common, so the decision walks far into the request
+    and races the bonus row; lengths are ragged, with some requests at the maximum."""
+    w = synth.scaled(synth.TOKEN_LARGE, B=24, gamma=gamma, V=6000, draft_noise=noise)
+    lens = synth.ragged_lengths(24, gamma, seed=21)
+    lens[:4] = gamma
+    inp = _to_dev(synth.token_inputs(w, device="cpu", draft_len=lens))
+    gpu, ref, _ = _parity(sv, orc, 0, inp)
+    if noise < 0.1:
+        assert (ref["accepted_len"] >= 16).sum() >= 4  # long runs were exercised
+
+
 def test_sampler_matches_oracle(sv, orc):
     """Draft tokens raced from q on the GPU equal the oracle's, except counted near-ties."""
     for w in (synth.TOKEN_SMALL, synth.scaled(synth.TOKEN_LARGE, B=16, V=50000)):

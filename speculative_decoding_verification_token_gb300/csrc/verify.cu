@@ -112,6 +112,7 @@ struct StreamParams {
   int32_t B, gmax, C;
   VerifyWs ws;
   int32_t* status;
+  int32_t clear_status;  // this launch resets the call's status word (see stream_kernel)
 };
 
 struct StageMeta {
@@ -287,8 +288,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(StreamParams 
   }
   // the race kernel that follows may launch now (it waits for this grid's results itself)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (blockIdx.x == 0)  // the race's per-request slots start empty
+  if (blockIdx.x == 0) {  // the race's per-request slots start empty
     for (int i = threadIdx.x; i < p.B; i += blockDim.x) p.ws.slots[i] = RaceSlot{0ull, 0u, 0u};
+    // The call's status word starts at SV_OK.  This kernel reports nothing but an expired wait,
+    // a second after its start, and the race kernel that follows waits for this grid before it
+    // reports anything, so clearing the word here orders it before every report of the call.
+    if (threadIdx.x == 0 && p.clear_status && p.status) *p.status = SV_OK;
+  }
   __syncthreads();
   if (warp == kConsumerWarps) {
     if ((threadIdx.x & 31) == 0) stream_producer<E>(p, ring, full, empty, meta);
@@ -1311,7 +1317,10 @@ static sv_status run_verify(bool block, const CommonArgs& a, const int64_t* targ
   const int32_t S = slices_of(a.V, esize<E>());
   const int32_t C = chunks_of(a.V, esize<E>());
   const VerifyWs ws = verify_layout(a.ws, a.B, a.gmax, C);
-  if (status && cudaMemsetAsync(status, 0, sizeof(int32_t), stream) != cudaSuccess)
+  // token-level verification with rows to stream clears the status word in its first kernel
+  const bool stream_clears = !block && int64_t(a.gmax) * a.B * C > 0;
+  if (status && !stream_clears &&
+      cudaMemsetAsync(status, 0, sizeof(int32_t), stream) != cudaSuccess)
     return SV_ERR_CUDA;
 
   const uint8_t* target = static_cast<const uint8_t*>(a.target);
@@ -1319,7 +1328,7 @@ static sv_status run_verify(bool block, const CommonArgs& a, const int64_t* targ
   DecideParams dp = {};
   sv_status st;
   if (!block) {
-    StreamParams sp;
+    StreamParams sp = {};
     sp.target = target;
     sp.draft = draft;
     sp.V = a.V;
@@ -1332,6 +1341,7 @@ static sv_status run_verify(bool block, const CommonArgs& a, const int64_t* targ
     sp.C = C;
     sp.ws = ws;
     sp.status = status;
+    sp.clear_status = stream_clears ? 1 : 0;
     profile_mark(0, stream);
     st = launch_stream<E>(sp, stream);
     if (st != SV_OK) return st;

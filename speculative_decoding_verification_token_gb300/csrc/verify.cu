@@ -343,12 +343,27 @@ __device__ __forceinline__ float resid_gap(float4 nm, float lnw) {
   return (nm.x - nm.z) * kLn2 + logf(nm.y / nm.w) - lnw;
 }
 
+// Drafted token x of position i of request r and its target and draft logits (lane 0 of a warp).
+template <typename E>
+__device__ __forceinline__ void fetch_drafted(const DecideParams& p, int32_t r, int32_t i,
+                                              int32_t& x, float& tx, float& dx) {
+  const int64_t drow = p.draft_row0[r] + (i - 1);
+  x = p.draft_tokens[drow];
+  tx = dx = 0.f;
+  if (x >= 0 && int64_t(x) < p.V) {
+    tx = Elem<E>::load(row_ptr<E>(p.target, p.target_row0[r] + (i - 1), p.ld), x);
+    dx = Elem<E>::load(row_ptr<E>(p.draft, drow, p.ld), x);
+  }
+}
+
 // The decision of request r by one CTA.  `writer`: this CTA writes the call's ratio outputs and
 // the status word; `s_desc` receives the race descriptor in shared memory.  Every thread of the
-// CTA must call it.
+// CTA must call it.  `dep_wait`: the caller is a programmatic dependent that has not yet waited
+// for the previous kernel (whose row partials this reads); the call's own inputs -- the ACCEPT
+// uniforms, each warp's first drafted token and its two logits -- are fetched before the wait.
 template <typename E>
 __device__ __noinline__ void decide_body(const DecideParams& p, int32_t r, bool writer,
-                                         RaceDesc* s_desc) {
+                                         RaceDesc* s_desc, bool dep_wait) {
   __shared__ float s_ratio[SV_MAX_DRAFT_LEN + 1];
   __shared__ float s_u[SV_MAX_DRAFT_LEN + 1];
   __shared__ float4 s_norm[SV_MAX_DRAFT_LEN + 1];
@@ -357,23 +372,23 @@ __device__ __noinline__ void decide_body(const DecideParams& p, int32_t r, bool 
   const int32_t graw = p.draft_len[r];
   const int32_t g = clamp_gamma(graw, p.gmax);
   const uint64_t req = p.request_ids ? p.request_ids[r] : uint64_t(r);
+  // uniforms u_i (ACCEPT tag, position i), one thread each
+  for (int i = tid + 1; i <= g; i += kThreads)
+    s_u[i] = uniform_of(stream_block(make_stream(p.seed, req, i, kTagAccept), 0).x);
+  int32_t x0 = -1;
+  float tx0 = 0.f, dx0 = 0.f;
+  if (lane == 0 && warp + 1 <= g) fetch_drafted<E>(p, r, warp + 1, x0, tx0, dx0);
+  if (dep_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) s_bad = (graw != g) ? SV_ERR_BAD_INPUT : 0;
   __syncthreads();
 
   // row normalisers and the drafted token's ratio, one warp per row
   for (int i = warp + 1; i <= g; i += kWarps) {
     const int32_t unit = r * p.gmax + (i - 1);
-    // lane 0 fetches the drafted token and its two logits while the warp folds the partials
-    const int64_t drow = p.draft_row0[r] + (i - 1);
-    int32_t x = -1;
-    float tx = 0.f, dx = 0.f;
-    if (lane == 0) {
-      x = p.draft_tokens[drow];
-      if (x >= 0 && int64_t(x) < p.V) {
-        tx = Elem<E>::load(row_ptr<E>(p.target, p.target_row0[r] + (i - 1), p.ld), x);
-        dx = Elem<E>::load(row_ptr<E>(p.draft, drow, p.ld), x);
-      }
-    }
+    // lane 0 has the drafted token and its two logits (fetched now past the first row)
+    int32_t x = x0;
+    float tx = tx0, dx = dx0;
+    if (lane == 0 && i != warp + 1) fetch_drafted<E>(p, r, i, x, tx, dx);
     float mt = kM2Empty, st = 0.f, md = kM2Empty, sd = 0.f;
     for (int c = lane; c < p.C; c += 32) {
       const float4 q = __ldcg(&p.ws.partials[size_t(unit) * p.C + c]);
@@ -390,9 +405,6 @@ __device__ __noinline__ void decide_body(const DecideParams& p, int32_t r, bool 
       s_norm[i] = make_float4(mt, st, md, sd);
     }
   }
-  // uniforms u_i (ACCEPT tag, position i), one thread each
-  for (int i = tid + 1; i <= g; i += kThreads)
-    s_u[i] = uniform_of(stream_block(make_stream(p.seed, req, i, kTagAccept), 0).x);
   __syncthreads();
 
   if (tid == 0) {
@@ -1078,8 +1090,10 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) race_kernel(RacePara
   const int tid = threadIdx.x;
   const int32_t job = blockIdx.x / p.CL;
   const int32_t part = blockIdx.x - job * p.CL;  // this CTA's share of the job's row
-  // launched as a programmatic dependent of the previous kernel: wait for its results
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // launched as a programmatic dependent of the previous kernel: wait for its results (the
+  // token-level decision waits inside decide_body, after fetching the call's own inputs)
+  const bool decide_here = !p.sampler && p.fused;
+  if (!decide_here) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // resolve the job
   bool active = true;
@@ -1091,7 +1105,7 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) race_kernel(RacePara
   if (!p.sampler) {
     r = job;
     if (p.fused) {
-      decide_body<E>(p.dp, r, part == 0, &s_desc);
+      decide_body<E>(p.dp, r, part == 0, &s_desc, true);
       __syncthreads();
     }
     const RaceDesc d = p.fused ? s_desc : p.ws.desc[r];

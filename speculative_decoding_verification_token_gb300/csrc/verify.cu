@@ -357,13 +357,13 @@ __device__ __forceinline__ void fetch_drafted(const DecideParams& p, int32_t r, 
 }
 
 // The decision of request r by one CTA.  `writer`: this CTA writes the call's ratio outputs and
-// the status word; `s_desc` receives the race descriptor in shared memory.  Every thread of the
-// CTA must call it.  `dep_wait`: the caller is a programmatic dependent that has not yet waited
+// the status word; `s_desc` receives the race descriptor and `s_tok` the drafted tokens (position
+// i at i - 1) in shared memory.  Every thread of the CTA must call it.  `dep_wait`: the caller is a programmatic dependent that has not yet waited
 // for the previous kernel (whose row partials this reads); the call's own inputs -- the ACCEPT
 // uniforms, each warp's first drafted token and its two logits -- are fetched before the wait.
 template <typename E>
 __device__ __noinline__ void decide_body(const DecideParams& p, int32_t r, bool writer,
-                                         RaceDesc* s_desc, bool dep_wait) {
+                                         RaceDesc* s_desc, int32_t* s_tok, bool dep_wait) {
   __shared__ float s_ratio[SV_MAX_DRAFT_LEN + 1];
   __shared__ float s_u[SV_MAX_DRAFT_LEN + 1];
   __shared__ float4 s_norm[SV_MAX_DRAFT_LEN + 1];
@@ -403,6 +403,7 @@ __device__ __noinline__ void decide_body(const DecideParams& p, int32_t r, bool 
       if (bad) s_bad = SV_ERR_BAD_INPUT;
       s_ratio[i] = ratio;
       s_norm[i] = make_float4(mt, st, md, sd);
+      s_tok[i - 1] = x;
     }
   }
   __syncthreads();
@@ -1087,6 +1088,7 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) race_kernel(RacePara
   __shared__ int32_t s_winner;
   __shared__ float s_k0;
   __shared__ RaceDesc s_desc;
+  __shared__ int32_t s_tok[SV_MAX_DRAFT_LEN];  // the request's drafted tokens (decided here)
   const int tid = threadIdx.x;
   const int32_t job = blockIdx.x / p.CL;
   const int32_t part = blockIdx.x - job * p.CL;  // this CTA's share of the job's row
@@ -1105,7 +1107,7 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) race_kernel(RacePara
   if (!p.sampler) {
     r = job;
     if (p.fused) {
-      decide_body<E>(p.dp, r, part == 0, &s_desc, true);
+      decide_body<E>(p.dp, r, part == 0, &s_desc, s_tok, true);
       __syncthreads();
     }
     const RaceDesc d = p.fused ? s_desc : p.ws.desc[r];
@@ -1203,7 +1205,7 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) race_kernel(RacePara
     int32_t* out = p.out_tokens + size_t(r) * p.out_ld;
     for (int64_t q = tid; q < p.out_ld; q += kThreads) {
       int32_t v = -1;
-      if (q < tau) v = p.draft_tokens[p.draft_row0[r] + q];
+      if (q < tau) v = p.fused ? s_tok[q] : p.draft_tokens[p.draft_row0[r] + q];
       else if (q == tau) v = y;
       out[q] = v;
     }

@@ -649,14 +649,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "token-level verify, 64 requests x 5 drafted positions + bonus, "
-                               "V=151936, bf16 logits (target N(0,9) + Zipf(1.1) prior, draft = "
-                               "target + N(0,1)), drafts sampled from q",
-                   "B": w.B, "gamma": w.gamma, "V": w.V,
-                   "l2": "inputs (213.9 MB) larger than L2, and L2 flushed before every step "
-                         "by a 512 MB write followed by a 256 MB read (no dirty flush lines "
-                         "left to write back inside the timed region)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": token_config(w, world),
         "positions_per_s": round(pos_s, 1),
         "hbm_frac_of_measured": round(res["bytes"] / res["t_mean"] / 1e9 / hbm, 4),
         "kernel_ms": {"stream": round(res["kernel_ms"][0], 4),
@@ -688,6 +681,18 @@ def main():
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def token_config(w, world):
+    """The workload both arms report (the reference arm times the CPU oracle on samples of it)."""
+    return {"workload": "token-level verify, 64 requests x 5 drafted positions + bonus, "
+                        "V=151936, bf16 logits (target N(0,9) + Zipf(1.1) prior, draft = "
+                        "target + N(0,1)), drafts sampled from q",
+            "B": w.B, "gamma": w.gamma, "V": w.V,
+            "l2": "inputs (213.9 MB) larger than L2, and L2 flushed before every step "
+                  "by a 512 MB write followed by a 256 MB read (no dirty flush lines "
+                  "left to write back inside the timed region)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def run_reference(args, rank, world):
@@ -735,9 +740,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "token-level verify, 64 requests x 5 drafted positions + "
-                                   "bonus, V=151936, bf16 logits", "B": w.B, "gamma": w.gamma,
-                       "V": w.V},
+            "config": token_config(w, world),
             "impl": "reference",
             "positions_per_s": round(w.gamma * n_req * args.steps / tot, 2),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,

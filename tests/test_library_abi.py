@@ -55,3 +55,27 @@ def test_invalid_arguments_rejected_before_launch(sv):
     assert call(ws_bytes=16) == sv.SV_ERR_INVALID                           # workspace too small
     assert L.dspark_schedule(None, None, 4, 4, None, 2, None, None, None, None, None, None, 0,
                              None) == sv.SV_ERR_INVALID
+
+
+def test_host_tensors_are_refused(sv):
+    """The binding has no CPU path: tensors in host memory are refused before anything is called,
+    for every entry point that computes."""
+    import torch
+    B, G, V = 2, 3, 64
+    t = torch.zeros((B * (G + 1), V), dtype=torch.float32)
+    d = torch.zeros((B * G, V), dtype=torch.float32)
+    t0 = torch.arange(B, dtype=torch.int64) * (G + 1)
+    d0 = torch.arange(B, dtype=torch.int64) * G
+    ln = torch.full((B,), G, dtype=torch.int32)
+    tok = torch.zeros(B * G, dtype=torch.int32)
+    with pytest.raises((ValueError, TypeError)):
+        sv.spec_verify_token(t, d, t0, d0, ln, G, tok, 0)
+    with pytest.raises((ValueError, TypeError)):
+        sv.spec_verify_block(t, d, t0, d0, ln, G, tok, 0)
+    with pytest.raises((ValueError, TypeError)):
+        sv.spec_sample_draft(d, d0, ln, G, 0)
+    c = torch.full((B, G), 0.5, dtype=torch.float32)
+    ml = torch.full((B,), G, dtype=torch.int32)
+    sps = torch.ones(16, dtype=torch.float64)
+    with pytest.raises((ValueError, TypeError)):
+        sv.dspark_schedule(c, ml, sps, 15)

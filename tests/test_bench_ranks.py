@@ -48,3 +48,24 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, 1, torch.device("cpu")) == 3.5
     assert bench.whole_job_rate(10, 4, 1, 2.0) == 20.0
+
+
+def test_reference_arm_prints_once_on_rank_zero(capsys):
+    """The reference arm (the CPU oracle on samples of the workload) runs and prints on rank 0
+    only; the other ranks return without work or output."""
+    import argparse
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    args = argparse.Namespace(steps=1, warmup=1, gpus=2, impl="reference")
+    bench.run_reference(args, 1, 2)
+    assert capsys.readouterr().out == ""
+    bench.run_reference(args, 0, 2)
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    from speculative_decoding_verification_token_gb300 import synth
+    assert line["config"] == bench.token_config(synth.TOKEN_LARGE, 2)
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0

@@ -167,10 +167,12 @@ sv_status spec_sample_draft(const void* draft_logits, sv_dtype dtype, int64_t V,
  * Scratch memory is a fixed array of SV_NOALLOC_SCRATCH_BYTES inside the library, held by every
  * GPU that loads the library until the process exits; calls whose
  * spec_verify_workspace_bytes(B, max_draft_len, V, dtype) exceeds it return SV_ERR_UNSUPPORTED.
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  Every call shares the one
- * array and clears the counters it needs before use, so calls that overlap on the GPU (other
- * streams or other host threads) race on it and produce undefined results. */
+ * The first call in each CUDA context (the current device's primary context, or a context the
+ * caller made current) looks up the array's device address (cudaGetSymbolAddress) and caches it
+ * by the context's id, so a device reset or a new context gets a fresh lookup; make that first
+ * call before any stream capture.  Every call shares the one array and clears the counters it
+ * needs before use, so calls that overlap on the GPU (other streams or other host threads) race
+ * on it and produce undefined results. */
 #define SV_NOALLOC_SCRATCH_BYTES (8u << 20)
 sv_status spec_verify_token_noalloc(const void* target_logits, const void* draft_logits,
                                     sv_dtype dtype, int64_t V, int64_t ld,

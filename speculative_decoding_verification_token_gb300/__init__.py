@@ -21,6 +21,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "specverify.h")
 SV_OK, SV_ERR_INVALID, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_BAD_INPUT, SV_ERR_TIMEOUT = range(6)
 SV_F32, SV_BF16 = 0, 1
 SV_MAX_DRAFT_LEN = 64
+SV_NOALLOC_SCRATCH_BYTES = 8 << 20  # scratch array of spec_verify_token_noalloc
 
 _lock = threading.Lock()
 _lib = None

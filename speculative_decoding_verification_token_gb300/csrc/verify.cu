@@ -24,6 +24,8 @@
 #include <algorithm>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "race.cuh"
 #include "sv_device.cuh"
 #include "sv_host.h"
@@ -1573,23 +1575,66 @@ constexpr size_t kNoAllocScratchBytes = SV_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device.  In host code the array's name is a
-// host-side stand-in, not a device address, so the address is looked up once per device (with
-// that device current) and cached.
+// Unique id of the CUDA context current on the calling thread, or 0 if there is none yet or the
+// driver cannot be asked.  The two driver calls are reached through the runtime's entry-point
+// query, so the library needs no link against the driver library.  Context ids are never reused
+// within a process, unlike context handles.
+static unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch in the current context.  In host code the array's name is
+// a host-side stand-in, not a device address, so the address is looked up with the context
+// current and cached by context id: a device reset or another context (a driver-API context of
+// an engine, say) gets a lookup of its own instead of a stale address.  Without a context id
+// (no driver entry points) every call looks the address up again.
 static sv_status noalloc_scratch_address(void** out) {
-  constexpr int kMaxDev = 64;
+  constexpr int kSlots = 64;
   static std::mutex mu;
-  static void* addr[kMaxDev] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return SV_ERR_CUDA;
+  static unsigned long long ids[kSlots] = {};
+  static void* addr[kSlots] = {};
+  static int next = 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return SV_ERR_CUDA;
-    addr[dev] = p;
+  unsigned long long id = current_context_id();
+  if (id != 0)
+    for (int k = 0; k < kSlots; ++k)
+      if (ids[k] == id) {
+        *out = addr[k];
+        return SV_OK;
+      }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    return SV_ERR_CUDA;
+  id = current_context_id();  // the lookup made the runtime's context current if none was
+  if (id != 0) {
+    ids[next] = id;
+    addr[next] = p;
+    next = (next + 1) % kSlots;
   }
-  *out = addr[dev];
+  *out = p;
   return SV_OK;
 }
 

@@ -2,14 +2,16 @@
 
 Policy: accepted lengths, emitted tokens and scheduler selections are compared bit for bit, except
 requests whose oracle decision margin |u - threshold| or race margin (best minus second-best key)
-is below 1e-5 -- those are counted and reported, never silently passed.  Probabilities (ratios,
-running ratios, thresholds) must agree within 1e-5 relative.
+is below 1e-5 -- those are counted and reported, never silently passed, and at most 1% of the
+requests (at least one) may differ on them.  Probabilities (ratios, running ratios, thresholds)
+must agree within 1e-5 relative.
 """
 import numpy as np
 import torch
 
 NEAR_TIE = 1e-5
 REL_TOL = 1e-5
+EXEMPT_FRAC = 0.01  # largest share of requests that may differ on exempt (near-tie) decisions
 RHO_PREC = 2e-6  # relative precision of a binary32 running ratio built from fp32 row sums
 R_ABS = 1e-6     # absolute precision of a binary32 residual mass (terms of size <= 2 in total)
 
@@ -92,6 +94,9 @@ def compare_verify(gpu, ref, block, lens, draft_row0, report=None):
             extra = {"max_rel_err_ratio": float(np.max(rel))}
     res = {"requests": int(acc.size), "exempt": int(exempt.sum()),
            "exempt_mismatch": int((mism & exempt).sum())}
+    # near ties may decide either way, but only a few of them can: more than 1% of the requests
+    # (at least one) differing on exempt decisions points at a systematic error, not at rounding
+    assert res["exempt_mismatch"] <= max(1, int(np.ceil(EXEMPT_FRAC * acc.size))), res
     if rows.size:
         res.update(extra)
     if report is not None:

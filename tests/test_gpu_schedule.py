@@ -235,3 +235,74 @@ def test_adaptive_round_on_device(sv, orc):
         assert (t_dev.cpu().numpy() == t_ref).all() and (a_dev.cpu().numpy() == a_ref).all()
         assert (upd["alpha"].cpu().numpy() == alpha1).all()
     print(f"\n[parity] adaptive round: {res}")
+
+
+def test_scheduled_round_full_size(sv, orc):
+    """The benchmark's scheduled round at full size: the device schedule of the 512 x 16
+    workload feeds token-level verification of V = 129280 bf16 rows laid out as the benchmark
+    lays them out (17 target and 16 draft rows per request, only the selected prefixes read), and
+    every request is compared with the oracle.  The oracle gets the selected rows only and runs
+    on all host threads (its C calls release the interpreter lock)."""
+    import concurrent.futures as cf
+    import os
+    sw = synth.SCHEDULE
+    si = synth.schedule_inputs(sw)
+    vw = synth.SCHEDULED_VERIFY
+    B, G, V = vw.B, vw.gamma, vw.V
+    vin = synth.token_inputs(vw, device="cuda")
+    sched = sv.dspark_schedule(torch.from_numpy(si["cond_accept"]).cuda(),
+                               torch.from_numpy(si["max_len"]).cuda(),
+                               torch.from_numpy(si["sps"]).cuda(), si["B_max"])
+    ref_s = orc.schedule(si["cond_accept"], si["max_len"], si["sps"], si["B_max"])
+    torch.cuda.synchronize()
+    sel = ref_s["sel_len"].astype(np.int32)
+    assert (sched["sel_len"].cpu().numpy() == sel).all()
+    # compact host copies of exactly the rows the verifier reads
+    t_rows = np.concatenate([np.arange(r * (G + 1), r * (G + 1) + sel[r] + 1) for r in range(B)])
+    d_rows = np.concatenate([np.arange(r * G, r * G + sel[r]) for r in range(B)])
+    tgt = vin["target"][torch.from_numpy(t_rows).cuda()].float().cpu().numpy()
+    drf = vin["draft"][torch.from_numpy(d_rows).cuda()].float().cpu().numpy()
+    t0 = np.concatenate([[0], np.cumsum(sel + 1)[:-1]]).astype(np.int64)
+    d0 = np.concatenate([[0], np.cumsum(sel)[:-1]]).astype(np.int64)
+    workers = os.cpu_count() or 1
+    chunks = [(a, min(B, a + 16)) for a in range(0, B, 16)]
+
+    def sample(ch):
+        a, b = ch
+        st, tok = orc.sample_draft_batch(drf, V, V, d0[a:b], sel[a:b], b - a, vw.seed,
+                                         request_ids=np.arange(a, b, dtype=np.uint64),
+                                         n_draft_rows=drf.shape[0])
+        assert st == 0
+        return tok
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        parts = list(ex.map(sample, chunks))
+    tok_c = np.max(np.stack(parts), axis=0).astype(np.int32)  # each row filled by one chunk
+    assert (tok_c >= 0).all()
+
+    def verify(ch):
+        a, b = ch
+        return orc.verify_batch(0, tgt, drf, V, V, t0[a:b], d0[a:b], sel[a:b], tok_c, b - a,
+                                vw.seed, request_ids=np.arange(a, b, dtype=np.uint64),
+                                out_ld=G + 1)
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        vparts = list(ex.map(verify, chunks))
+    assert all(p["status"] == 0 for p in vparts)
+    ref = {k: np.concatenate([p[k] for p in vparts])
+           for k in ("accepted_len", "out_tokens", "decision_margin", "race_margin")}
+    ratio = np.full(B * G, np.nan)
+    for (a, b), p in zip(chunks, vparts):
+        for r in range(a, b):
+            ratio[r * G: r * G + sel[r]] = p["ratio"][d0[r]: d0[r] + sel[r]]
+    ref["ratio"] = ratio
+    # the device chain: scheduler lengths straight into the verifier, full row layout
+    tokens = np.zeros(B * G, np.int32)
+    tokens[d_rows] = tok_c
+    gpu = sv.spec_verify_token(vin["target"], vin["draft"], vin["target_row0"],
+                               vin["draft_row0"], sched["sel_len"], G,
+                               torch.from_numpy(tokens).cuda(), vw.seed)
+    torch.cuda.synchronize()
+    assert int(gpu["status"].item()) == 0
+    res = compare_verify(gpu, ref, 0, sel, np.arange(B, dtype=np.int64) * G)
+    print(f"\n[parity] scheduled round, 512 x 16, V = {V}: {res}, "
+          f"{int(sel.sum())} drafted positions verified")
+    assert res["requests"] == B

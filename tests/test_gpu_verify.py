@@ -176,10 +176,11 @@ def test_sampler_matches_oracle(sv, orc):
         d = _to_dev(inp)
         got = sv.spec_sample_draft(d["draft"], d["draft_row0"], d["draft_len"],
                                    d["max_draft_len"], d["seed"]).cpu().numpy()
-        assert (got == ref).mean() > 0.99
-        # every mismatch must be a near-tie of the oracle's race
+        # every mismatch must be a near-tie of the oracle's race, and near ties are rare
         draft = host_f32(inp["draft"])
-        for row in np.flatnonzero(got != ref):
+        miss = np.flatnonzero(got != ref)
+        assert miss.size <= max(1, int(np.ceil(0.01 * ref.size))), miss
+        for row in miss:
             r, i = divmod(int(row), w.gamma)
             st, tok, margin = orc.sample_race(draft[row], w.seed, r, i + 1, orc.TAG_DRAFT)
             assert tok == ref[row] and margin < 1e-5
@@ -242,3 +243,50 @@ def test_empty_batch_and_argument_errors(sv):
     with pytest.raises(sv.SpecVerifyError):
         sv.spec_verify_token(z, z, i64, i64, i32, sv.SV_MAX_DRAFT_LEN + 1,
                              torch.zeros(1, dtype=torch.int32, device="cuda"), 0)
+
+
+def _residual_empty_batch(orc, B, gamma, V, dtype, seed):
+    """Requests whose correction residual is empty to working precision on both sides.
+
+    Request r % 3 == 0: position 1 is degenerate -- the target masks the drafted token x
+    (p(x) = 0) and the draft gives it the logit -120 (weight ~e^-120, lost when added to a
+    normaliser of order one in binary32 and binary64), every other entry equal in both rows; so
+    p(x)/q(x) = 0 rejects x and max(p - q, 0) is empty.  Request r % 3 == 1: position 1 has equal
+    target and draft rows (ratio exactly 1, always accepted; for block verification R_1 = 0 and
+    R_1 + 1 - rho_1 = 0, so h_1 = 1) and position 2 is degenerate.  Request r % 3 == 2: ordinary
+    rows.  Returns the inputs, the drafted tokens and the requests expected to fall back."""
+    w = synth.scaled(synth.TOKEN_LARGE, B=B, gamma=gamma, V=V, dtype=dtype)
+    inp = synth.token_inputs(w, device="cpu")
+    tokens = oracle_tokens(orc, inp)
+    rng = np.random.default_rng(seed)
+    t, d = inp["target"], inp["draft"]
+    fall = []
+    for r in range(B):
+        kind = r % 3
+        if kind == 2:
+            continue
+        pos = 1 if kind == 0 else 2
+        if kind == 1:
+            d[r * gamma] = t[r * (gamma + 1)]  # position 1: draft row = target row
+        trow, drow = r * (gamma + 1) + pos - 1, r * gamma + pos - 1
+        x = int(rng.integers(V // 2, V))
+        d[drow] = t[trow]
+        t[trow, x] = float("-inf")
+        d[drow, x] = -120.0
+        tokens[drow] = x
+        fall.append(r)
+    return inp, tokens, np.array(fall)
+
+
+@pytest.mark.parametrize("block", [0, 1])
+@pytest.mark.parametrize("dtype,V", [(torch.bfloat16, 20000), (torch.float32, 4099)])
+def test_residual_empty_fallback(sv, orc, block, dtype, V):
+    """An empty residual at the first rejection: both sides draw the correction from p with the
+    RESID uniforms of that position (the oracle reports the fallback), token for token."""
+    inp, tokens, fall = _residual_empty_batch(orc, 12, 3, V, dtype, seed=17)
+    dev = _padded_dev(inp) if (V * inp["target"].element_size()) % 16 else _to_dev(inp)
+    gpu, ref, res = _parity(sv, orc, block, dev, tokens=tokens)
+    kinds = ref["race_kind"]
+    assert (kinds[fall] == orc.RACE_RESIDUAL_EMPTY).all(), kinds
+    assert (ref["accepted_len"][fall] == fall % 3).all()
+    assert res["exempt_mismatch"] == 0

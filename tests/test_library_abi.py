@@ -79,3 +79,11 @@ def test_host_tensors_are_refused(sv):
     sps = torch.ones(16, dtype=torch.float64)
     with pytest.raises((ValueError, TypeError)):
         sv.dspark_schedule(c, ml, sps, 15)
+
+
+def test_noalloc_scratch_size_matches_header(sv):
+    """The binding's SV_NOALLOC_SCRATCH_BYTES is the header's."""
+    import re
+    with open(sv.HEADER) as f:
+        m = re.search(r"#define\s+SV_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", f.read())
+    assert m and int(m.group(1)) << int(m.group(2)) == sv.SV_NOALLOC_SCRATCH_BYTES

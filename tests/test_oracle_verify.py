@@ -187,8 +187,9 @@ def test_edge_cases(orc):
         assert res.status == 0 and res.correction >= 10
 
 
-def test_residual_empty_fallback(orc):
-    """p and q equal to working precision: the residual is empty, the correction comes from p."""
+def test_identical_rows_accept_and_bonus(orc):
+    """p = q: the ratio is exactly one, every draft is accepted (u < 1 always) and the emitted
+    token after the draft is the bonus token, drawn from the target's next row."""
     V = 6
     t = np.log(np.full(V, 1.0 / V)).astype(np.float32)
     rows = np.stack([t, t])
@@ -196,6 +197,48 @@ def test_residual_empty_fallback(orc):
     for req in range(2000):
         res, ratio = orc.verify_token_request(rows, t[None], [2], 5, req)
         assert ratio[0] == 1.0
-        assert res.accepted_len == 1  # u < 1 = rho always
+        assert res.accepted_len == 1 and res.race_kind == orc.RACE_BONUS
         seen.add(res.correction)
     assert seen == set(range(V))
+
+
+def residual_empty_rows(V, x, seed):
+    """One drafted position whose residual max(p - q, 0) is empty to working precision.
+
+    The target masks token x (p(x) = 0) and the draft gives it the logit -120, a weight of
+    about e^-120 of the row's scale; every other entry is the same in both rows.  So the ratio
+    p(x)/q(x) is 0 (x is always rejected), and adding e^-120 to a normaliser of order one leaves it
+    unchanged in binary64 and binary32 alike: p(y) = q(y) exactly for every y != x."""
+    rng = np.random.default_rng(seed)
+    t = rng.normal(0.0, 1.0, V).astype(np.float32)
+    d = t.copy()
+    t[x] = -np.inf
+    d[x] = -120.0
+    return t, d
+
+
+@pytest.mark.parametrize("block", [0, 1])
+def test_residual_empty_fallback(orc, block):
+    """Rejection with an empty residual: the correction falls back to a race over p with the RESID
+    uniforms of the rejected position, so the emitted token is distributed as p (chi-square over
+    4000 requests), and x, which p excludes, never comes out."""
+    from scipy.stats import chisquare
+    V, x, n = 8, 5, 4000
+    t, d = residual_empty_rows(V, x, seed=41)
+    rows_t = np.stack([t, t])  # position 1 and the bonus row
+    counts = np.zeros(V)
+    for req in range(n):
+        if block:
+            res, rho, h = orc.verify_block_request(rows_t, d[None], [x], 7, req)
+            assert rho[0] == 0.0 and h[0] == 0.0
+        else:
+            res, ratio = orc.verify_token_request(rows_t, d[None], [x], 7, req)
+            assert ratio[0] == 0.0
+        assert res.status == 0 and res.accepted_len == 0
+        assert res.race_kind == orc.RACE_RESIDUAL_EMPTY
+        counts[res.correction] += 1
+    assert counts[x] == 0
+    p = softmax(t.astype(np.float64))
+    keep = p > 0
+    stat = chisquare(counts[keep], n * p[keep] / p[keep].sum())
+    assert stat.pvalue > 1e-4, (counts, n * p)

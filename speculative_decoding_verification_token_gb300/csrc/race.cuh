@@ -232,7 +232,8 @@ __device__ __forceinline__ void race_range(const RaceSpec& rs, const uint4* vsrc
   }
 }
 
-// CTA-wide winner (every thread receives it).
+// CTA-wide winner (every thread receives it) of a CTA of NT threads.
+template <int NT = kThreads>
 __device__ __forceinline__ void block_race(float& key, int32_t& idx, float* red_k,
                                            int32_t* red_i) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -245,7 +246,7 @@ __device__ __forceinline__ void block_race(float& key, int32_t& idx, float* red_
   float k = red_k[0];
   int32_t i = red_i[0];
 #pragma unroll
-  for (int w = 1; w < kWarps; ++w)
+  for (int w = 1; w < NT / 32; ++w)
     if (race_better(red_k[w], red_i[w], k, i)) {
       k = red_k[w];
       i = red_i[w];
@@ -255,6 +256,7 @@ __device__ __forceinline__ void block_race(float& key, int32_t& idx, float* red_
   idx = i;
 }
 
+template <int NT = kThreads>
 __device__ __forceinline__ float block_max(float v, float* red_k) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   v = warp_max(v);
@@ -262,19 +264,19 @@ __device__ __forceinline__ float block_max(float v, float* red_k) {
   __syncthreads();
   float m = red_k[0];
 #pragma unroll
-  for (int w = 1; w < kWarps; ++w) m = fmaxf(m, red_k[w]);
+  for (int w = 1; w < NT / 32; ++w) m = fmaxf(m, red_k[w]);
   __syncthreads();
   return m;
 }
 
-// Race over a whole row by one CTA (rare fallback path; no pruning).
-template <typename E>
+// Race over a whole row by one CTA of NT threads (rare fallback path; no pruning).
+template <typename E, int NT = kThreads>
 __device__ void race_row_global(const RaceSpec& rs, const uint8_t* trow, const uint8_t* drow,
                                 int64_t V, float* red_k, int32_t* red_i, float& out_key,
                                 int32_t& out_idx) {
   float bk = -INFINITY;
   int32_t bi = -1;
-  for (int64_t e = threadIdx.x; e < V; e += kThreads) {
+  for (int64_t e = threadIdx.x; e < V; e += NT) {
     const float x = Elem<E>::load(trow, e);
     const float d = rs.resid ? Elem<E>::load(drow, e) : 0.f;
     if (!race_active(rs, x, d)) continue;
@@ -284,7 +286,7 @@ __device__ void race_row_global(const RaceSpec& rs, const uint8_t* trow, const u
       bi = int32_t(e);
     }
   }
-  block_race(bk, bi, red_k, red_i);
+  block_race<NT>(bk, bi, red_k, red_i);
   out_key = bk;
   out_idx = bi;
 }

@@ -522,7 +522,8 @@ def bench_block(steps, warmup, flush, stream):
     st_tok = int(status.item())
     acc = holder["o"]["accepted_len"].cpu()
     t_rows = time_calls(blk(True), steps, warmup, flush, stream)
-    # device duration of the tokens-only call's one kernel (statistics, residuals, decision, race)
+    # device durations of the tokens-only call's kernels: the row-statistics stream, the prep and
+    # residual-mass kernels, the decision and race (events between them: serialised)
     sv.sv_profile_enable(True)
     parts = []
     call = blk(False)
@@ -539,7 +540,8 @@ def bench_block(steps, warmup, flush, stream):
     return {
         "ms": tm * 1e3, "GB_s": nb / tm / 1e9, "positions_per_s": w.B * w.gamma / tm,
         "ms_with_row_outputs": tr * 1e3, "GB_s_with_row_outputs": nb / tr / 1e9,
-        "kernel_ms": {"block_kernel": round(kms[0], 4)},
+        "kernel_ms": {"stream": round(kms[0], 4), "prep_and_residuals": round(kms[1], 4),
+                      "decide_and_race": round(kms[2], 4)},
         "mean_accepted": float(acc.float().mean()),
         "status": st_tok or int(status.item())}
 

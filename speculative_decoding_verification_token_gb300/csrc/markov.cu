@@ -204,6 +204,9 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   if (warp == 0) {
     // ---- producer
     if (lane == 0) {
+      // Wt is read again at every position and by both M-blocks: keep it in L2 ahead of the
+      // backbone, which is read once
+      const uint64_t keep = tc::policy_evict_last(), once = tc::policy_evict_first();
       for (int t = 0; t < n_my; ++t) {
         const int32_t n = ci + t * p.per_mblock;
         const int s = t % kMkStages;
@@ -211,11 +214,12 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         if (t >= kMkStages && !mbar_wait(&b_empty[s], (use - 1) & 1, p.status)) break;
         mbar_expect_tx(&b_full[s], kMkBBytes);
         for (int kb = 0; kb < kMkKB; ++kb)
-          tc::tma_load_2d(sB + s * kMkBBytes + kb * (kMkCols * 128), &map_wt, kb * 64,
-                          n * kMkCols, &b_full[s]);
+          tc::tma_load_2d_hint(sB + s * kMkBBytes + kb * (kMkCols * 128), &map_wt, kb * 64,
+                               n * kMkCols, &b_full[s], keep);
         if (t >= kMkStages && !mbar_wait(&bb_empty[s], (use - 1) & 1, p.status)) break;
         mbar_expect_tx(&bb_full[s], kMkBBBytes);
-        tc::tma_load_3d(sBB + s * kMkBBBytes, &map_bb, n * kMkCols, p.k - 1, m0, &bb_full[s]);
+        tc::tma_load_3d_hint(sBB + s * kMkBBBytes, &map_bb, n * kMkCols, p.k - 1, m0, &bb_full[s],
+                             once);
       }
     }
   } else if (warp == 1) {
@@ -245,14 +249,15 @@ __global__ void __launch_bounds__(kMkThreads, 1)
     // store its four 32 x 64 quadrant blocks; once the stores of tile t - 1 have read their
     // buffer, hand that buffer back to the epilogue
     if (lane == 0 && p.write_z) {
+      const uint64_t once = tc::policy_evict_first();  // z is written once, read by the caller
       for (int t = 0; t < n_my; ++t) {
         const int32_t n = ci + t * p.per_mblock;
         const int zb = t % kMkZBufs;
         if (!mbar_wait(&z_full[zb], (t / kMkZBufs) & 1, p.status)) break;
         for (int q = 0; q < 4; ++q)
           if (m0 + 32 * q < p.B)  // a block wholly past B has nothing to store
-            tc::tma_store_3d(&map_z, sZ + (zb * 4 + q) * kMkZGroupBytes, n * kMkCols, p.k - 1,
-                             m0 + 32 * q);
+            tc::tma_store_3d_hint(&map_z, sZ + (zb * 4 + q) * kMkZGroupBytes, n * kMkCols,
+                                  p.k - 1, m0 + 32 * q, once);
         tc::bulk_commit();
         tc::bulk_wait_read<1>();
         if (t > 0) mbar_arrive(&z_empty[(t - 1) % kMkZBufs]);

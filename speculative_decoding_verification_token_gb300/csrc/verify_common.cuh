@@ -35,10 +35,29 @@ struct RaceSlot {                 // per race job: the shares' combined winner
   uint32_t k0;                    // key_order of the best seed key published so far (0: none)
 };
 
+constexpr int32_t kResShareBytes = 16384;  // bytes of one row in one residual-mass task
+
+// Block verification's per-request state between its kernels.  Residual masses are computed for
+// "slots": round-1 slots [0, count[0]) are listed by the prep kernel, round-2 slots
+// [units, units + count[1]) by the round-1 kernel.
+struct BlockWs {
+  float4* norm;    // [units] row-pair normalisers (m_t, s_t, m_d, s_d), log2 domain
+  float* rho;      // [units] running ratio rho_i
+  float* eta;      // [units] ACCEPT uniform eta_i
+  int32_t* cand;   // [units] slot of (r, i), -1 if R_i is not computed
+  int32_t* unit;   // [2 units] unit (r * gmax + i - 1) of each slot
+  int32_t* done;   // [units] round-1 slots: shares finished
+  int32_t* count;  // [2] slots listed for round 1 and round 2
+  float* rpart;    // [2 units * CLr] residual mass partials, one per (slot, share)
+  int32_t units;   // B * gmax: the first round-2 slot
+  int32_t CLr;     // residual tasks (shares) per row
+};
+
 struct VerifyWs {
-  float4* partials;  // [units * C] (m_t, s_t, m_d, s_d), m in log2 units (token-level)
+  float4* partials;  // [units * C] (m_t, s_t, m_d, s_d), m in log2 units
   RaceDesc* desc;    // [B]
   RaceSlot* slots;   // [units]: verify uses B of them, the sampler one per drafted row
+  BlockWs blk;
   size_t total;
 };
 
@@ -55,7 +74,14 @@ static inline int32_t chunks_of(int64_t V, int esz) {
   return static_cast<int32_t>((V + per - 1) / per);
 }
 
-static inline VerifyWs verify_layout(void* base, int32_t B, int32_t gmax, int32_t C) {
+// Residual-mass tasks per row: one per kResShareBytes of the row.
+static inline int32_t resid_shares_of(int64_t V, int esz) {
+  const int64_t per = kResShareBytes / esz;
+  return static_cast<int32_t>((V + per - 1) / per);
+}
+
+static inline VerifyWs verify_layout(void* base, int32_t B, int32_t gmax, int64_t V, int esz) {
+  const int32_t C = chunks_of(V, esz);
   VerifyWs w;
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
@@ -69,12 +95,22 @@ static inline VerifyWs verify_layout(void* base, int32_t B, int32_t gmax, int32_
   w.partials = reinterpret_cast<float4*>(take(sizeof(float4) * units * size_t(C)));
   w.desc = reinterpret_cast<RaceDesc*>(take(sizeof(RaceDesc) * Bn));
   w.slots = reinterpret_cast<RaceSlot*>(take(sizeof(RaceSlot) * units));
+  w.blk.CLr = resid_shares_of(V, esz);
+  w.blk.units = static_cast<int32_t>(units);
+  w.blk.norm = reinterpret_cast<float4*>(take(sizeof(float4) * units));
+  w.blk.rho = reinterpret_cast<float*>(take(sizeof(float) * units));
+  w.blk.eta = reinterpret_cast<float*>(take(sizeof(float) * units));
+  w.blk.cand = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * units));
+  w.blk.unit = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * 2 * units));
+  w.blk.done = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * units));
+  w.blk.count = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * 2));
+  w.blk.rpart = reinterpret_cast<float*>(take(sizeof(float) * 2 * units * size_t(w.blk.CLr)));
   w.total = off;
   return w;
 }
 
 static inline size_t verify_ws_bytes(int32_t B, int32_t gmax, int64_t V, int esz) {
-  return verify_layout(nullptr, B, gmax, chunks_of(V, esz)).total;
+  return verify_layout(nullptr, B, gmax, V, esz).total;
 }
 
 __device__ __forceinline__ int32_t clamp_gamma(int32_t g, int32_t gmax) {

@@ -13,7 +13,10 @@ NEAR_TIE = 1e-5
 REL_TOL = 1e-5
 EXEMPT_FRAC = 0.01  # largest share of requests that may differ on exempt (near-tie) decisions
 RHO_PREC = 2e-6  # relative precision of a binary32 running ratio built from fp32 row sums
-R_ABS = 1e-6     # absolute precision of a binary32 residual mass (terms of size <= 2 in total)
+# absolute precision of a binary32 residual mass R: every term max(rho p - q, 0) carries the
+# rounding of its two exponentials and of one fma (about 3 * 2^-22 of rho p), and the terms of rho p
+# add up to at most rho <= 1, so |dR| < 7.2e-7 plus the summation's rounding
+R_ABS = 1e-6
 
 
 def host_f32(t):

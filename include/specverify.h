@@ -263,6 +263,26 @@ sv_status dspark_schedule_rule(const float* cond_accept, const int32_t* max_len,
                                double* objective, int32_t* status, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/* Asynchronous scheduling with confidences from two rounds before ("DeepSeek Boosts Inference
+ * Speed by 85%", "The Third Ace": at production speed the scheduler cannot wait for the current
+ * step's confidence, so it schedules with the predictions of two steps before, and the admission
+ * never depends on the token it admits; "DSpark: DeepSeek's bet on speed that doesn't betray
+ * quality", "Verifying only what matters": the same, for the reference capacity).
+ * conf_ring: DEVICE fp32 [depth][N][K], depth >= 3, a ring of confidence-head outputs: round t's
+ * predictions go to slot t % depth (for instance dspark_markov_draft's conf_out pointed there).
+ * Round t (>= 0) is scheduled with slot (t - 2) % depth, the predictions made two rounds before
+ * for request slot i and position k; the first two rounds, which have none, with cond_prior
+ * (DEVICE fp32 [N][K], for instance dspark_acceptance_update's estimates).  The scheduling itself
+ * -- stopping rule, order, fixed-point sums, arguments, outputs, errors, workspace -- is
+ * dspark_schedule_rule's.  The call reads nothing written for rounds t and t - 1, so it can run on
+ * a stream that waits only for round t - 2's confidence head, concurrently with round t's draft. */
+sv_status dspark_schedule_async(const float* conf_ring, int32_t depth, int64_t round,
+                                const float* cond_prior, const int32_t* max_len, int32_t N,
+                                int32_t K, const double* sps, int32_t B_max, int32_t rule,
+                                int32_t* sel_len, float* survival, int32_t* total_rows,
+                                double* objective, int32_t* status, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
 /* Per-position acceptance learned while serving ("How much does a token cost", "Adaptive
  * verification": a drafter without a confidence head gets a per-position trust level estimated
  * from the tokens verification accepted).  One verified round: request i verified its first

@@ -79,6 +79,7 @@ def _load():
                                                    u64, P, P, P, P, P, P]),
             "orc_schedule": (C.c_int, [P, P, i32, i32, P, i32, P, P, P, P]),
             "orc_schedule_rule": (C.c_int, [P, P, i32, i32, P, i32, i32, P, P, P, P]),
+            "orc_schedule_async": (C.c_int, [P, i64, P, P, i32, i32, P, i32, i32, P, P, P, P]),
             "orc_acceptance_update": (C.c_int, [P, P, i32, i32, f64, f64, f64, P, P, P]),
             "orc_sts_fit": (C.c_int, [P, P, P, i32, i32, i32, f64, f64, i32, P, P, P, P, P]),
         }
@@ -279,6 +280,26 @@ def schedule(cond_accept, max_len, sps, B_max, rule=STOP_FIRST_DROP):
     st = _load().orc_schedule_rule(c.ctypes.data, ml.ctypes.data, N, K, sps.ctypes.data, B_max,
                                    int(rule), sel.ctypes.data, surv.ctypes.data, C.byref(total),
                                    C.byref(obj))
+    return {"status": st, "sel_len": sel, "survival": surv, "total_rows": total.value,
+            "objective": obj.value}
+
+
+def schedule_async(conf_rounds, round_, prior, max_len, sps, B_max, rule=STOP_FIRST_DROP):
+    """Round `round_` scheduled with the predictions of round `round_` - 2 (conf_rounds
+    [rounds, N, K]; prior [N, K] for rounds 0 and 1)."""
+    conf = _f32(conf_rounds)
+    prior = _f32(prior)
+    _, N, K = conf.shape
+    ml = _arr(max_len, np.int32)
+    sps = np.ascontiguousarray(sps, dtype=np.float64)
+    sel = np.zeros(N, dtype=np.int32)
+    surv = np.zeros((N, K), dtype=np.float32)
+    total = C.c_int32()
+    obj = C.c_double()
+    st = _load().orc_schedule_async(conf.ctypes.data, int(round_), prior.ctypes.data,
+                                    ml.ctypes.data, N, K, sps.ctypes.data, B_max, int(rule),
+                                    sel.ctypes.data, surv.ctypes.data, C.byref(total),
+                                    C.byref(obj))
     return {"status": st, "sel_len": sel, "survival": surv, "total_rows": total.value,
             "objective": obj.value}
 

@@ -630,6 +630,18 @@ int orc_schedule(const float* cond_accept, const int32_t* max_len, int32_t N, in
                            survival, total_rows, objective);
 }
 
+/* ---- asynchronous scheduling: predictions from two rounds before ------------------------------ */
+
+int orc_schedule_async(const float* conf_rounds, int64_t round, const float* prior,
+                       const int32_t* max_len, int32_t N, int32_t K, const double* sps,
+                       int32_t B_max, int32_t rule, int32_t* sel_len, float* survival,
+                       int32_t* total_rows, double* objective) {
+  if (round < 0) return ORC_ERR_ARGS;
+  const float* cond = round >= 2 ? conf_rounds + (size_t)(round - 2) * (size_t)N * (size_t)K : prior;
+  return orc_schedule_rule(cond, max_len, N, K, sps, B_max, rule, sel_len, survival, total_rows,
+                           objective);
+}
+
 /* ---- online per-position acceptance ----------------------------------------------------------- */
 
 int orc_acceptance_update(const int32_t* sel_len, const int32_t* accepted_len, int32_t N,

@@ -208,6 +208,17 @@ int orc_schedule_rule(const float* cond_accept, const int32_t* max_len, int32_t 
                       const double* sps, int32_t B_max, int32_t rule, int32_t* sel_len,
                       float* survival, int32_t* total_rows, double* objective);
 
+/* Asynchronous scheduling ("DeepSeek Boosts Inference Speed by 85%", "The Third Ace"; "DSpark:
+ * DeepSeek's bet on speed that doesn't betray quality", "Verifying only what matters"): the
+ * scheduler of round t uses the confidence predictions made two rounds before, so its admission
+ * never depends on the token it admits.  conf_rounds [rounds][N][K] holds each round's predictions;
+ * round t is scheduled by orc_schedule_rule with conf_rounds[t - 2] when t >= 2, with prior [N][K]
+ * for rounds 0 and 1 (no prediction is two rounds old yet). */
+int orc_schedule_async(const float* conf_rounds, int64_t round, const float* prior,
+                       const int32_t* max_len, int32_t N, int32_t K, const double* sps,
+                       int32_t B_max, int32_t rule, int32_t* sel_len, float* survival,
+                       int32_t* total_rows, double* objective);
+
 /* Per-position acceptance learned while serving ([TC] "Adaptive verification": a drafter without a
  * confidence head gets a per-position trust level estimated from the tokens verification
  * accepted).  Request i verified its first sel_len[i] drafted tokens and accepted the first

@@ -72,6 +72,8 @@ def lib():
             "dspark_schedule_workspace_bytes": (sz, [i32, i32]),
             "dspark_schedule": (st, [P, P, i32, i32, P, i32, P, P, P, P, P, P, sz, P]),
             "dspark_schedule_rule": (st, [P, P, i32, i32, P, i32, i32, P, P, P, P, P, P, sz, P]),
+            "dspark_schedule_async": (st, [P, i32, i64, P, P, i32, i32, P, i32, i32, P, P, P, P, P,
+                                           P, sz, P]),
             "dspark_acceptance_update": (st, [P, P, i32, i32, C.c_double, C.c_double, C.c_double,
                                               P, P, P, P, P, P]),
             "dspark_sts_fit": (st, [P, P, P, i32, i32, i32, C.c_double, C.c_double, i32, P, P, P,
@@ -330,6 +332,34 @@ def dspark_schedule(cond_accept, max_len, sps, B_max, want_survival=True, status
                                       _ptr(obj), _ptr(status), _ptr(ws), ws.numel(),
                                       _stream(stream))
     _check(code, "dspark_schedule_rule")
+    return {"sel_len": sel, "survival": surv, "total_rows": total, "objective": obj,
+            "status": status}
+
+
+def dspark_schedule_async(conf_ring, round_, cond_prior, max_len, sps, B_max, rule=SV_STOP_FIRST_DROP,
+                          want_survival=True, status=None, workspace=None, stream=None):
+    """Round `round_` scheduled with the confidences of round `round_` - 2: conf_ring fp32
+    [depth >= 3, N, K] (round t's confidence head writes slot t % depth), cond_prior fp32 [N, K] for
+    the first two rounds; otherwise as dspark_schedule."""
+    _dev(conf_ring, torch.float32), _dev(cond_prior, torch.float32)
+    _dev(max_len, torch.int32), _dev(sps, torch.float64)
+    depth, N, K = conf_ring.shape
+    if tuple(cond_prior.shape) != (N, K):
+        raise ValueError("cond_prior must be [N, K] like one ring slot")
+    dev = conf_ring.device
+    sel = torch.empty(N, dtype=torch.int32, device=dev)
+    surv = torch.empty((N, K), dtype=torch.float32, device=dev) if want_survival else None
+    total = torch.empty(1, dtype=torch.int32, device=dev)
+    obj = torch.empty(1, dtype=torch.float64, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    need = dspark_schedule_workspace_bytes(N, K)
+    ws = workspace if workspace is not None else globals()["workspace"](need, dev)
+    code = lib().dspark_schedule_async(_ptr(conf_ring), int(depth), int(round_), _ptr(cond_prior),
+                                       _ptr(max_len), N, K, _ptr(sps), int(B_max), int(rule),
+                                       _ptr(sel), _ptr(surv), _ptr(total), _ptr(obj),
+                                       _ptr(status), _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "dspark_schedule_async")
     return {"sel_len": sel, "survival": surv, "total_rows": total, "objective": obj,
             "status": status}
 

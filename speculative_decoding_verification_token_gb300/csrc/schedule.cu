@@ -607,6 +607,26 @@ extern "C" sv_status dspark_schedule(const float* cond_accept, const int32_t* ma
 }
 
 // ---------------------------------------------------------------------------------------------
+// dspark_schedule_async: round t scheduled with the confidences of round t - 2
+// ---------------------------------------------------------------------------------------------
+extern "C" sv_status dspark_schedule_async(const float* conf_ring, int32_t depth, int64_t round,
+                                           const float* cond_prior, const int32_t* max_len,
+                                           int32_t N, int32_t K, const double* sps,
+                                           int32_t B_max, int32_t rule, int32_t* sel_len,
+                                           float* survival, int32_t* total_rows,
+                                           double* objective, int32_t* status, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  if (depth < 3 || round < 0) return SV_ERR_INVALID;
+  if (N > 0 && K > 0 && (!conf_ring || !cond_prior)) return SV_ERR_INVALID;
+  // slot (t - 2) % depth holds the predictions made two rounds before; slots t % depth and
+  // (t - 1) % depth, which rounds t and t - 1 write, are never read
+  const float* cond = cond_prior;
+  if (round >= 2) cond = conf_ring + size_t((round - 2) % depth) * size_t(N) * size_t(K);
+  return dspark_schedule_rule(cond, max_len, N, K, sps, B_max, rule, sel_len, survival,
+                              total_rows, objective, status, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------------------------------------
 // dspark_acceptance_update: per-position acceptance counts from one verified round
 // ---------------------------------------------------------------------------------------------
 namespace sv {

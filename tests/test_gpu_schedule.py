@@ -306,3 +306,50 @@ def test_scheduled_round_full_size(sv, orc):
     print(f"\n[parity] scheduled round, 512 x 16, V = {V}: {res}, "
           f"{int(sel.sum())} drafted positions verified")
     assert res["requests"] == B
+
+
+def test_schedule_async_two_stream_chain(sv, orc):
+    """Six rounds of the asynchronous scheduler on the device.  A "draft" stream writes each
+    round's confidence-head predictions into slot t % 3 of a ring; a "schedule" stream schedules
+    round t from slot (t - 2) % 3, waiting only for round t - 2's write (and the draft stream
+    overwrites a slot only after the schedule that reads it).  Every round's selection, total and
+    objective equal the oracle's chain bit for bit."""
+    rng = np.random.default_rng(23)
+    N, K, T, depth = 96, 8, 6, 3
+    conf = (rng.beta(8, 2, (T, N, K)) * 0.97 ** np.arange(K)).astype(np.float32)
+    prior = np.full((N, K), 0.75, np.float32)
+    ml = rng.integers(0, K + 1, N).astype(np.int32)
+    B_max = N * (K + 1)
+    sps = 1.0 / (2e-3 + np.arange(B_max + 1) * 4e-6)
+    dev = torch.device("cuda")
+    ring = torch.zeros((depth, N, K), dtype=torch.float32, device=dev)
+    host = torch.from_numpy(conf).pin_memory()
+    prior_d = torch.from_numpy(prior).to(dev)
+    ml_d = torch.from_numpy(ml).to(dev)
+    sps_d = torch.from_numpy(sps).to(dev)
+    torch.cuda.synchronize()
+    s_draft, s_sched = torch.cuda.Stream(), torch.cuda.Stream()
+    written = [torch.cuda.Event() for _ in range(T)]
+    read = [torch.cuda.Event() for _ in range(T)]
+    outs = []
+    for t in range(T):
+        with torch.cuda.stream(s_draft):
+            if t >= depth:  # slot t % 3 was last read by the schedule of round t - 1
+                s_draft.wait_event(read[t - 1])
+            ring[t % depth].copy_(host[t], non_blocking=True)
+            written[t].record(s_draft)
+        with torch.cuda.stream(s_sched):
+            if t >= 2:
+                s_sched.wait_event(written[t - 2])
+            outs.append(sv.dspark_schedule_async(ring, t, prior_d, ml_d, sps_d, B_max,
+                                                 stream=s_sched))
+            read[t].record(s_sched)
+    torch.cuda.synchronize()
+    for t, o in enumerate(outs):
+        ref = orc.schedule_async(conf, t, prior, ml, sps, B_max)
+        assert ref["status"] == 0 and int(o["status"].item()) == 0
+        assert (o["sel_len"].cpu().numpy() == ref["sel_len"]).all(), t
+        assert int(o["total_rows"].item()) == ref["total_rows"]
+        assert float(o["objective"].item()) == ref["objective"]
+    # the selections change from round to round: the chain really reads different slots
+    assert len({tuple(o["sel_len"].cpu().numpy()) for o in outs[2:]}) > 1

@@ -313,3 +313,45 @@ def test_best_budget_dominates_fixed_depth(orc, seed):
     best = orc.schedule(c, max_len, sps, B_max, rule=orc.STOP_ARGMAX)
     fixed = orc.schedule(c, max_len, sps, B_max, rule=orc.STOP_FIXED_DEPTH)
     assert best["objective"] >= fixed["objective"]
+
+
+# ---- asynchronous scheduling: predictions from two rounds before -----------------------------
+
+def test_schedule_async_three_rounds_by_hand(orc):
+    """Two requests, one drafted position each, SPS = 1.0, 0.8, 0.7 at 2, 3, 4 verification rows.
+    f(b) = (2 + first b survival values) * SPS(2 + b); admission stops at the first f(b + 1) <=
+    f(b).  Rounds 0 and 1 have no two-rounds-old prediction and use the prior 0.3: f(1) = 2.3 *
+    0.8 = 1.84 < 2 admits nothing.  Round 2 uses round 0's predictions (0.9, 0.6): f = 2, 2.32,
+    3.5 * 0.7 = 2.45, both admitted.  Round 3 uses round 1's (0.2, 0.95): f = 2, 2.36, 2.205 --
+    request 1 only.  Round 4 uses round 2's (0.1, 0.1): nothing."""
+    prior = np.array([[0.3], [0.3]], np.float32)
+    conf = np.array([[[0.9], [0.6]], [[0.2], [0.95]], [[0.1], [0.1]], [[0.99], [0.99]],
+                     [[0.5], [0.5]]], np.float32)
+    sps = np.array([1.0, 1.0, 1.0, 0.8, 0.7])
+    want = {0: ([0, 0], 2), 1: ([0, 0], 2), 2: ([1, 1], 4), 3: ([0, 1], 3), 4: ([0, 0], 2)}
+    for t, (sel, rows) in want.items():
+        out = orc.schedule_async(conf, t, prior, [1, 1], sps, 4)
+        assert out["status"] == 0
+        assert list(out["sel_len"]) == sel and out["total_rows"] == rows, (t, out)
+    assert orc.schedule_async(conf, 2, prior, [1, 1], sps, 4)["objective"] == pytest.approx(2.45)
+
+
+def test_schedule_async_is_causal(orc):
+    """Round t's selection does not depend on the predictions of rounds t and t - 1 (the tokens
+    it admits), only on those of round t - 2."""
+    rng = np.random.default_rng(17)
+    N, K, T = 40, 6, 6
+    conf = (rng.beta(8, 2, (T, N, K)) * 0.97 ** np.arange(K)).astype(np.float32)
+    prior = np.full((N, K), 0.7, np.float32)
+    ml = rng.integers(0, K + 1, N).astype(np.int32)
+    sps = 1.0 / (2e-3 + np.arange(N * (K + 1) + 1) * 4e-6)
+    for t in range(T):
+        ref = orc.schedule_async(conf, t, prior, ml, sps, N * (K + 1))
+        poked = conf.copy()
+        poked[t] = 1.0 - poked[t]
+        if t >= 1:
+            poked[t - 1] = 0.0
+        got = orc.schedule_async(poked, t, prior, ml, sps, N * (K + 1))
+        assert (got["sel_len"] == ref["sel_len"]).all() and got["objective"] == ref["objective"]
+        base = orc.schedule(conf[t - 2] if t >= 2 else prior, ml, sps, N * (K + 1))
+        assert (base["sel_len"] == ref["sel_len"]).all()

@@ -185,6 +185,62 @@ sv_status spec_verify_token_noalloc(const void* target_logits, const void* draft
                                     int32_t* status, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Token-level verification with the vocabulary split across ranks (tensor parallelism over the
+ * vocabulary, as in the vocabulary-parallel serving of "How much does a token cost",
+ * "Experiments").  A rank holds columns [v_off, v_off + Vs) of every logit row (v_off a multiple
+ * of 8; V_total the whole vocabulary); rows, tokens and layout are those of spec_verify_token
+ * with V = Vs, and draft tokens are global vocabulary ids.  Softmax statistics merge across shards
+ * by log-sum-exp and the exponential race keys every entry by its global index, so the result
+ * equals spec_verify_token's over the whole vocabulary.  A round is four calls and two exchanges
+ * that the caller makes between ranks (all-gathers, in rank = shard order):
+ *   spec_verify_shard_stats   per drafted row pair (request r, position i at r * max_draft_len +
+ *                             i - 1): row_stats DEVICE fp32 [B * max_draft_len][4] = this shard's
+ *                             (m_t, s_t, m_d, s_d), m in log2 units (max * log2 e), s = sum of
+ *                             2^(x log2 e - m); token_logits DEVICE fp32 [B * max_draft_len][2] =
+ *                             the drafted token's target and draft logits if the shard holds it,
+ *                             -inf otherwise.  Workspace: spec_verify_workspace_bytes(B,
+ *                             max_draft_len, Vs, dtype).
+ *   -- all-gather both arrays over the shards: [n_shards][rows][4] and [n_shards][rows][2]
+ *   spec_verify_shard_merge   the shards' statistics merged in shard order, the token logits of
+ *                             the shard that holds each token (the same on every rank).
+ *   spec_verify_shard_race    every request decided as spec_verify_token does (accepted_len[B],
+ *                             accept_ratio as there), then this shard's race of the correction
+ *                             (or bonus) row: winners DEVICE uint64 [B][2] = the shard's best
+ *                             (order-preserving key bits << 32 | ~global index), and, when the
+ *                             shard holds no positive residual entry, its best for the race over p
+ *                             with the same uniforms (else 0).
+ *   -- all-gather winners: [n_shards][B][2]
+ *   spec_verify_shard_finish  the largest winner over the shards (the race over p's if no shard
+ *                             had a residual entry, as spec_verify_token falls back) and the
+ *                             outputs out_tokens / correction_token of spec_verify_token.
+ * Each call resets `status` and reports data errors as spec_verify_token does. */
+sv_status spec_verify_shard_stats(const void* target_logits, const void* draft_logits,
+                                  sv_dtype dtype, int64_t Vs, int64_t ld, int64_t v_off,
+                                  int64_t V_total, const int64_t* target_row0,
+                                  const int64_t* draft_row0, const int32_t* draft_len,
+                                  int32_t max_draft_len, const int32_t* draft_tokens, int32_t B,
+                                  float* row_stats, float* token_logits, int32_t* status,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+sv_status spec_verify_shard_merge(const float* row_stats_all, const float* token_logits_all,
+                                  int32_t n_shards, int64_t rows, float* row_stats,
+                                  float* token_logits, void* stream);
+sv_status spec_verify_shard_race(const void* target_logits, const void* draft_logits,
+                                 sv_dtype dtype, int64_t Vs, int64_t ld, int64_t v_off,
+                                 int64_t V_total, const int64_t* target_row0,
+                                 const int64_t* draft_row0, const int32_t* draft_len,
+                                 int32_t max_draft_len, const int32_t* draft_tokens, int32_t B,
+                                 uint64_t seed, const uint64_t* request_ids,
+                                 const float* row_stats, const float* token_logits,
+                                 int32_t* accepted_len, float* accept_ratio, uint64_t* winners,
+                                 int32_t* status, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+sv_status spec_verify_shard_finish(const uint64_t* winners_all, int32_t n_shards, int32_t B,
+                                   const int32_t* accepted_len, const int64_t* draft_row0,
+                                   const int32_t* draft_tokens, int32_t* out_tokens,
+                                   int64_t out_ld, int32_t* correction_token, int32_t* status,
+                                   void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * DSpark draft side.
  * ------------------------------------------------------------------------------------------- */
 

@@ -69,6 +69,8 @@ def _load():
             "orc_speedup": (f64, [f64, C.c_int, f64]),
             "orc_sample_race": (C.c_int, [P, i64, u64, u64, u32, u32, P, P]),
             "orc_sample_draft_batch": (C.c_int, [P, i64, i64, P, P, i32, u64, P, P]),
+            "orc_race_shard": (C.c_int, [P, P, i64, i64, C.c_int, f64, f64, f64, f64, f64,
+                                         u64, u64, u32, u32, P, P]),
             "orc_verify_token_request": (C.c_int, [P, P, i64, i64, P, i32, u64, u64, P, P]),
             "orc_verify_block_request": (C.c_int, [P, P, i64, i64, P, i32, u64, u64, P, P, P]),
             "orc_verify_batch": (C.c_int, [C.c_int, P, P, i64, i64, P, P, P, P, i32, u64, P, P,
@@ -165,6 +167,19 @@ def sample_draft_batch(draft, V, ld, draft_row0, draft_len, B, seed, request_ids
                                         draft_len.ctypes.data, B, seed, _p(rids),
                                         tokens.ctypes.data)
     return st, tokens
+
+
+def race_shard(trow, drow, v_off, resid, w, stats, seed, req, pos, tag):
+    """Best (key, global index) of the race over the vocabulary shard trow / drow (columns
+    v_off ..), with the whole rows' statistics stats = (Mt, St, Md, Sd) (natural log)."""
+    trow = _f32(trow)
+    drow = _f32(drow) if drow is not None else trow
+    key, idx = C.c_double(), C.c_int64()
+    Mt, St, Md, Sd = (float(v) for v in stats)
+    _load().orc_race_shard(trow.ctypes.data, drow.ctypes.data, trow.size, int(v_off), int(resid),
+                           float(w), Mt, St, Md, Sd, seed, req, pos, tag, C.byref(key),
+                           C.byref(idx))
+    return key.value, idx.value
 
 
 # ---- verification ----------------------------------------------------------------------------

@@ -176,6 +176,29 @@ int orc_sample_draft_batch(const float* draft, int64_t V, int64_t ld, const int6
   return ORC_OK;
 }
 
+/* Race over one vocabulary shard, columns [v_off, v_off + Vs) of a row pair, with the row's
+ * whole-vocabulary statistics: weight w p(x) - q(x) when resid (else p(x)), the key of column x
+ * keyed by the uniform of its global index v_off + x.  Returns the shard's best key and its global
+ * index (-1 if no entry carries weight).  The shards' best keys combine by maximum (lowest index
+ * among equals) into the race over the whole row ("How much does a token cost", "Experiments":
+ * vocabulary-parallel serving). */
+int orc_race_shard(const float* trow, const float* drow, int64_t Vs, int64_t v_off, int resid,
+                   double w, double Mt, double St, double Md, double Sd, uint64_t seed,
+                   uint64_t req, uint32_t pos, uint32_t tag, double* key, int64_t* index) {
+  race_t r;
+  race_init(&r);
+  for (int64_t x = 0; x < Vs; ++x) {
+    double weight = resid ? w * prob(trow, x, Mt, St) - prob(drow, x, Md, Sd)
+                          : prob(trow, x, Mt, St);
+    if (!(weight > 0.0)) continue;
+    race_offer(&r, log(weight) + race_noise(seed, req, pos, tag, (uint64_t)(v_off + x)),
+               v_off + x);
+  }
+  *key = r.best;
+  *index = r.arg;
+  return ORC_OK;
+}
+
 /* ---- verification -------------------------------------------------------------------------- */
 
 static int check_tokens(const int32_t* tokens, int32_t gamma, int64_t V) {

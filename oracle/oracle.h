@@ -122,6 +122,13 @@ typedef struct {
  * At the first rejection sample the correction from max(p_i - q_i, 0) (RESID tag, pos i) and stop;
  * if all are accepted sample the bonus token from p_{gamma+1} (BONUS tag, pos gamma+1).
  * accept_ratio (nullable, gamma entries) receives min(1, rho_i) for EVERY drafted position. */
+/* Race over one vocabulary shard, columns [v_off, v_off + Vs) of a row pair, with the row's
+ * whole-vocabulary statistics (natural log: M = max, S = sum exp(x - M)); uniforms keyed by the
+ * global index.  Best key and global index out ("How much does a token cost", "Experiments"). */
+int orc_race_shard(const float* trow, const float* drow, int64_t Vs, int64_t v_off, int resid,
+                   double w, double Mt, double St, double Md, double Sd, uint64_t seed,
+                   uint64_t req, uint32_t pos, uint32_t tag, double* key, int64_t* index);
+
 int orc_verify_token_request(const float* target, const float* draft, int64_t V, int64_t ld,
                              const int32_t* tokens, int32_t gamma, uint64_t seed, uint64_t req,
                              double* accept_ratio, orc_verify_result* res);

@@ -71,6 +71,12 @@ def lib():
                                          P, P, i64, P, P, P, P, sz, P]),
             "dspark_schedule_workspace_bytes": (sz, [i32, i32]),
             "dspark_schedule": (st, [P, P, i32, i32, P, i32, P, P, P, P, P, P, sz, P]),
+            "spec_verify_shard_stats": (st, [P, P, st, i64, i64, i64, i64, P, P, P, i32, P, i32,
+                                             P, P, P, P, sz, P]),
+            "spec_verify_shard_merge": (st, [P, P, i32, i64, P, P, P]),
+            "spec_verify_shard_race": (st, [P, P, st, i64, i64, i64, i64, P, P, P, i32, P, i32,
+                                            u64, P, P, P, P, P, P, P, P, sz, P]),
+            "spec_verify_shard_finish": (st, [P, i32, i32, P, P, P, P, i64, P, P, P]),
             "dspark_schedule_rule": (st, [P, P, i32, i32, P, i32, i32, P, P, P, P, P, P, sz, P]),
             "dspark_schedule_async": (st, [P, i32, i64, P, P, i32, i32, P, i32, i32, P, P, P, P, P,
                                            P, sz, P]),
@@ -256,6 +262,125 @@ def spec_sample_draft(draft, draft_row0, draft_len, max_draft_len, seed, request
                                    _stream(stream))
     _check(code, "spec_sample_draft")
     return draft_tokens
+
+
+# ---- vocabulary-sharded verification ------------------------------------------------------------
+
+def spec_verify_shard_stats(target, draft, v_off, V_total, target_row0, draft_row0, draft_len,
+                            max_draft_len, draft_tokens, status=None, workspace=None, stream=None):
+    """This shard's statistics of every drafted row pair and the drafted tokens' logits (-inf
+    where the shard does not hold the token).  Returns (stats fp32 [B * gmax, 4], tok fp32
+    [B * gmax, 2])."""
+    _dev(target, rows=True), _dev(draft, rows=True)
+    _dev(target_row0, torch.int64), _dev(draft_row0, torch.int64)
+    _dev(draft_len, torch.int32), _dev(draft_tokens, torch.int32)
+    dt = _dtype_code(target)
+    Vs, ld = target.shape[-1], target.stride(0)
+    B = draft_len.numel()
+    dev = target.device
+    units = max(1, B * max_draft_len)
+    stats = torch.empty((units, 4), dtype=torch.float32, device=dev)
+    tok = torch.empty((units, 2), dtype=torch.float32, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    need = spec_verify_workspace_bytes(B, max_draft_len, Vs, dt)
+    ws = workspace if workspace is not None else globals()["workspace"](need, dev)
+    code = lib().spec_verify_shard_stats(_ptr(target), _ptr(draft), dt, Vs, ld, int(v_off),
+                                         int(V_total), _ptr(target_row0), _ptr(draft_row0),
+                                         _ptr(draft_len), int(max_draft_len), _ptr(draft_tokens),
+                                         B, _ptr(stats), _ptr(tok), _ptr(status), _ptr(ws),
+                                         ws.numel(), _stream(stream))
+    _check(code, "spec_verify_shard_stats")
+    return stats, tok
+
+
+def spec_verify_shard_merge(stats_all, tok_all, stream=None):
+    """Statistics of every shard ([n, rows, 4]) merged in shard order; drafted-token logits
+    ([n, rows, 2]) from the shard that holds each token."""
+    _dev(stats_all, torch.float32), _dev(tok_all, torch.float32)
+    n, rows = stats_all.shape[0], stats_all.shape[1]
+    stats = torch.empty((rows, 4), dtype=torch.float32, device=stats_all.device)
+    tok = torch.empty((rows, 2), dtype=torch.float32, device=stats_all.device)
+    code = lib().spec_verify_shard_merge(_ptr(stats_all.contiguous()), _ptr(tok_all.contiguous()),
+                                         n, rows, _ptr(stats), _ptr(tok), _stream(stream))
+    _check(code, "spec_verify_shard_merge")
+    return stats, tok
+
+
+def spec_verify_shard_race(target, draft, v_off, V_total, target_row0, draft_row0, draft_len,
+                           max_draft_len, draft_tokens, seed, stats, tok, request_ids=None,
+                           want_ratio=True, status=None, workspace=None, stream=None):
+    """Every request decided from the merged statistics, then this shard's race.  Returns
+    {"accepted_len", "winners" (int64 [B, 2], unsigned bit patterns), "accept_ratio", "status"}."""
+    _dev(target, rows=True), _dev(draft, rows=True), _dev(request_ids)
+    dt = _dtype_code(target)
+    Vs, ld = target.shape[-1], target.stride(0)
+    B = draft_len.numel()
+    dev = target.device
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    winners = torch.empty((B, 2), dtype=torch.int64, device=dev)
+    ratio = (torch.empty(draft_tokens.numel(), dtype=torch.float32, device=dev)
+             if want_ratio else None)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    need = spec_verify_workspace_bytes(B, max_draft_len, Vs, dt)
+    ws = workspace if workspace is not None else globals()["workspace"](need, dev)
+    code = lib().spec_verify_shard_race(_ptr(target), _ptr(draft), dt, Vs, ld, int(v_off),
+                                        int(V_total), _ptr(target_row0), _ptr(draft_row0),
+                                        _ptr(draft_len), int(max_draft_len), _ptr(draft_tokens),
+                                        B, int(seed), _ptr(request_ids), _ptr(stats), _ptr(tok),
+                                        _ptr(acc), _ptr(ratio), _ptr(winners), _ptr(status),
+                                        _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "spec_verify_shard_race")
+    return {"accepted_len": acc, "winners": winners, "accept_ratio": ratio, "status": status}
+
+
+def spec_verify_shard_finish(winners_all, accepted_len, draft_row0, draft_tokens, out_ld,
+                             status=None, stream=None):
+    """The largest winner over the shards ([n, B, 2]) and the request outputs."""
+    _dev(winners_all, torch.int64), _dev(accepted_len, torch.int32)
+    n, B = winners_all.shape[0], winners_all.shape[1]
+    dev = winners_all.device
+    out = torch.empty((B, out_ld), dtype=torch.int32, device=dev)
+    corr = torch.empty(B, dtype=torch.int32, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    code = lib().spec_verify_shard_finish(_ptr(winners_all.contiguous()), n, B,
+                                          _ptr(accepted_len), _ptr(draft_row0),
+                                          _ptr(draft_tokens), _ptr(out), int(out_ld),
+                                          _ptr(corr), _ptr(status), _stream(stream))
+    _check(code, "spec_verify_shard_finish")
+    return {"out_tokens": out, "correction": corr, "accepted_len": accepted_len,
+            "status": status}
+
+
+def all_gather_stacked(t, group=None):
+    """The tensor t of every rank of `group`, stacked in rank order (the shard order)."""
+    import torch.distributed as dist
+    parts = [torch.empty_like(t) for _ in range(dist.get_world_size(group))]
+    dist.all_gather(parts, t.contiguous(), group=group)
+    return torch.stack(parts)
+
+
+def spec_verify_token_sharded(target, draft, v_off, V_total, target_row0, draft_row0, draft_len,
+                              max_draft_len, draft_tokens, seed, request_ids=None, out_ld=None,
+                              gather=all_gather_stacked, steps=None):
+    """Token-level verification of this rank's vocabulary shard (columns v_off .. v_off + Vs of
+    every row), rank r holding shard r: the four library calls with the two exchanges between
+    them, `gather(t)` stacking every rank's t in rank order (all_gather over the default process
+    group by default).  `steps` replaces the four calls (a dict with keys stats, merge, race,
+    finish taking the same arguments) -- the exchanges stay the same."""
+    st = steps or {"stats": spec_verify_shard_stats, "merge": spec_verify_shard_merge,
+                   "race": spec_verify_shard_race, "finish": spec_verify_shard_finish}
+    stats, tok = st["stats"](target, draft, v_off, V_total, target_row0, draft_row0, draft_len,
+                             max_draft_len, draft_tokens)
+    stats, tok = st["merge"](gather(stats), gather(tok))
+    race = st["race"](target, draft, v_off, V_total, target_row0, draft_row0, draft_len,
+                      max_draft_len, draft_tokens, seed, stats, tok, request_ids=request_ids)
+    out = st["finish"](gather(race["winners"]), race["accepted_len"], draft_row0, draft_tokens,
+                       out_ld or max_draft_len + 1)
+    out["accept_ratio"] = race.get("accept_ratio")
+    return out
 
 
 # ---- DSpark draft side ------------------------------------------------------------------------

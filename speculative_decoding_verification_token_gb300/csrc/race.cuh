@@ -35,6 +35,8 @@ struct RaceSpec {
   bool resid;
   float gap;
   Stream st;
+  int64_t off = 0;  // vocabulary index of the row's first entry (a vocabulary shard's offset, a
+                    // multiple of 8); the uniforms are keyed by the global index off + e
 };
 
 __device__ __forceinline__ float race_key(const RaceSpec& rs, float t, float d, float noise) {
@@ -54,7 +56,7 @@ __device__ __noinline__ float exact_key_t(const RaceSpec& rs, float t, const uin
                                           int64_t e) {
   const float d = rs.resid ? Elem<E>::load(drow, e) : 0.f;
   if (!race_active(rs, t, d)) return -INFINITY;
-  const uint4 b = stream_block(rs.st, static_cast<uint32_t>(e >> 2));
+  const uint4 b = stream_block(rs.st, static_cast<uint32_t>((e + rs.off) >> 2));
   return race_key(rs, t, d, race_noise(uniform_of(word_of(b, static_cast<uint32_t>(e & 3)))));
 }
 
@@ -211,8 +213,9 @@ __device__ __forceinline__ void race_range(const RaceSpec& rs, const uint4* vsrc
       const float tmax = vec_max<E>(a[u]);
       if (!(tmax >= floor_t)) continue;
       // e is a multiple of kPer (>= 4): the vector's words are whole Philox blocks
-      const uint4 b0 = stream_block(rs.st, static_cast<uint32_t>(e >> 2));
-      const uint4 b1 = kPer == 8 ? stream_block(rs.st, static_cast<uint32_t>(e >> 2) + 1) : b0;
+      const uint4 b0 = stream_block(rs.st, static_cast<uint32_t>((e + rs.off) >> 2));
+      const uint4 b1 =
+          kPer == 8 ? stream_block(rs.st, static_cast<uint32_t>((e + rs.off) >> 2) + 1) : b0;
       const uint32_t wmax = max(max(max(b0.x, b0.y), max(b0.z, b0.w)),
                                 max(max(b1.x, b1.y), max(b1.z, b1.w)));
       if (gate_m(wmax) > gate_threshold(tmax, c)) continue;
@@ -227,7 +230,7 @@ __device__ __forceinline__ void race_range(const RaceSpec& rs, const uint4* vsrc
     const int64_t e = e0 + i;
     const float x = Elem<E>::load(trow, e);
     if (!(x >= floor_t)) continue;
-    const uint4 b = stream_block(rs.st, static_cast<uint32_t>(e >> 2));
+    const uint4 b = stream_block(rs.st, static_cast<uint32_t>((e + rs.off) >> 2));
     offer<E>(rs, trow, drow, e, x, word_of(b, static_cast<uint32_t>(e & 3)), c, bk, bi);
   }
 }

@@ -255,6 +255,8 @@ struct DecideParams {
   float* ratio_out;  // min(1, p/q) per drafted row (nullable)
   VerifyWs ws;
   int32_t* status;
+  const float2* tok;  // nullable: the drafted tokens' (target, draft) logits per row pair, for a
+                      // vocabulary shard that may not hold them (V is then the whole vocabulary)
 };
 
 // Drafted token x of position i of request r and its target and draft logits (lane 0 of a warp).
@@ -265,8 +267,14 @@ __device__ __forceinline__ void fetch_drafted(const DecideParams& p, int32_t r, 
   x = p.draft_tokens[drow];
   tx = dx = 0.f;
   if (x >= 0 && int64_t(x) < p.V) {
-    tx = Elem<E>::load(row_ptr<E>(p.target, p.target_row0[r] + (i - 1), p.ld), x);
-    dx = Elem<E>::load(row_ptr<E>(p.draft, drow, p.ld), x);
+    if (p.tok) {
+      const float2 v = p.tok[size_t(r) * p.gmax + (i - 1)];
+      tx = v.x;
+      dx = v.y;
+    } else {
+      tx = Elem<E>::load(row_ptr<E>(p.target, p.target_row0[r] + (i - 1), p.ld), x);
+      dx = Elem<E>::load(row_ptr<E>(p.draft, drow, p.ld), x);
+    }
   }
 }
 
@@ -383,6 +391,8 @@ struct RaceParams {
   VerifyWs ws;
   int32_t* status;
   int32_t stage_share;      // the launch provides dynamic shared memory for the row share
+  int64_t v_off;            // vocabulary index of column 0 (a vocabulary shard; 0 otherwise)
+  unsigned long long* winners;  // nullable: a shard's race, [B][2] packed winners, not outputs
   DecideParams dp;          // token-level decision
   BlockDecideParams bd;     // block decision
 };
@@ -473,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) race_kernel(RacePara
   const uint8_t* drow = rs.resid ? row_ptr<E>(p.draft, p.draft_row0[r] + tau, p.ld) : nullptr;
   const uint64_t req = p.request_ids ? p.request_ids[r] : uint64_t(r);
   rs.st = make_stream(p.seed, req, uint32_t(tau + 1), rs.resid ? kTagResid : kTagBonus);
+  rs.off = p.v_off;
 
   // this CTA's share of the row: a contiguous range, a whole number of 16-byte vectors long
   constexpr int32_t kPer = Elem<E>::kPerVec;
@@ -531,6 +542,28 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) race_kernel(RacePara
   }
   __syncthreads();
   int32_t y = s_winner;
+  if (p.winners) {
+    // a vocabulary shard: this shard's winner with its global index, and -- if the shard holds no
+    // positive residual entry -- the shard's winner of the race over p with the same uniforms,
+    // which the request takes if no shard holds one (the residual is then empty everywhere)
+    unsigned long long fb_best = 0ull;
+    if (y < 0 && rs.resid) {
+      RaceSpec fb = rs;
+      fb.resid = false;
+      float k;
+      int32_t yf;
+      race_row_global<E>(fb, trow, nullptr, p.V, red_k, red_i, k, yf);
+      if (yf >= 0) fb_best = race_pack(k, int32_t(p.v_off + yf));
+    }
+    if (tid == 0) {
+      const unsigned long long best = atomicAdd(&slot->best, 0ull);
+      p.winners[2 * size_t(r)] =
+          best ? race_pack(key_from_order(uint32_t(best >> 32)), int32_t(p.v_off + y)) : 0ull;
+      p.winners[2 * size_t(r) + 1] = fb_best;
+      p.accepted_len[r] = tau;
+    }
+    return;
+  }
   if (y < 0 && rs.resid) {
     // residual empty to working precision (p and q agree): draw from p with the same uniforms
     RaceSpec fb = rs;

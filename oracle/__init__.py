@@ -69,6 +69,7 @@ def _load():
             "orc_speedup": (f64, [f64, C.c_int, f64]),
             "orc_sample_race": (C.c_int, [P, i64, u64, u64, u32, u32, P, P]),
             "orc_sample_draft_batch": (C.c_int, [P, i64, i64, P, P, i32, u64, P, P]),
+            "orc_lmhead_logits": (C.c_int, [P, P, i64, i64, i64, P]),
             "orc_race_shard": (C.c_int, [P, P, i64, i64, C.c_int, f64, f64, f64, f64, f64,
                                          u64, u64, u32, u32, P, P]),
             "orc_verify_token_request": (C.c_int, [P, P, i64, i64, P, i32, u64, u64, P, P]),
@@ -167,6 +168,17 @@ def sample_draft_batch(draft, V, ld, draft_row0, draft_len, B, seed, request_ids
                                         draft_len.ctypes.data, B, seed, _p(rids),
                                         tokens.ctypes.data)
     return st, tokens
+
+
+def lmhead_logits(hidden, W):
+    """Logits of hidden [rows, H] through W [V, H]: binary64 sums rounded once to binary32."""
+    hidden, W = _f32(hidden), _f32(W)
+    rows, H = hidden.shape
+    V = W.shape[0]
+    out = np.zeros((rows, V), dtype=np.float32)
+    st = _load().orc_lmhead_logits(hidden.ctypes.data, W.ctypes.data, rows, H, V, out.ctypes.data)
+    assert st == OK
+    return out
 
 
 def race_shard(trow, drow, v_off, resid, w, stats, seed, req, pos, tag):

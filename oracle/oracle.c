@@ -199,6 +199,23 @@ int orc_race_shard(const float* trow, const float* drow, int64_t Vs, int64_t v_o
   return ORC_OK;
 }
 
+/* ---- logits from hidden states ------------------------------------------------------------- */
+
+/* The output projection ("How much does a token cost", "The Role of Arithmetic Intensity": inputs
+ * [Q, H] times weights [H, W] give the Q x W logits): logits[i][v] = sum_j hidden[i][j] W[v][j],
+ * the products and their sum in binary64, rounded once to binary32. */
+int orc_lmhead_logits(const float* hidden, const float* W, int64_t rows, int64_t H, int64_t V,
+                      float* logits) {
+  if (rows < 0 || H <= 0 || V <= 0) return ORC_ERR_ARGS;
+  for (int64_t i = 0; i < rows; ++i)
+    for (int64_t v = 0; v < V; ++v) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < H; ++j) acc += (double)hidden[i * H + j] * (double)W[v * H + j];
+      logits[i * V + v] = (float)acc;
+    }
+  return ORC_OK;
+}
+
 /* ---- verification -------------------------------------------------------------------------- */
 
 static int check_tokens(const int32_t* tokens, int32_t gamma, int64_t V) {

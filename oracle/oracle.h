@@ -129,6 +129,12 @@ int orc_race_shard(const float* trow, const float* drow, int64_t Vs, int64_t v_o
                    double w, double Mt, double St, double Md, double Sd, uint64_t seed,
                    uint64_t req, uint32_t pos, uint32_t tag, double* key, int64_t* index);
 
+/* Logits of hidden-state rows through an output projection ("How much does a token cost", "The
+ * Role of Arithmetic Intensity"): logits[i][v] = sum_j hidden[i][j] W[v][j] in binary64, rounded
+ * once to binary32.  hidden [rows][H], W [V][H], logits [rows][V]. */
+int orc_lmhead_logits(const float* hidden, const float* W, int64_t rows, int64_t H, int64_t V,
+                      float* logits);
+
 int orc_verify_token_request(const float* target, const float* draft, int64_t V, int64_t ld,
                              const int32_t* tokens, int32_t gamma, uint64_t seed, uint64_t req,
                              double* accept_ratio, orc_verify_result* res);

@@ -121,3 +121,20 @@ def test_sts_confidence_matches_expit(orc):
     s = np.sort(rng.normal(0, 2, 20))
     c = [orc.sts_confidence(x, 1.3) for x in s]
     assert all(a < b for a, b in zip(c, c[1:]))
+
+
+def test_lmhead_logits_pins(orc):
+    """The output projection: a hand-worked 1 x 2 case, and random bf16-valued operands equal to
+    a binary64 matrix product rounded once to binary32 (the operands' products are exact in
+    binary64, so only the summation order differs: well inside one binary32 rounding)."""
+    h = np.array([[1.0, 2.0, -0.5]], np.float32)
+    W = np.array([[0.5, 0.25, 2.0], [-1.0, 1.0, 4.0]], np.float32)
+    assert orc.lmhead_logits(h, W).tolist() == [[0.0, -1.0]]  # 0.5+0.5-1, -1+2-2
+    import torch
+    rng = np.random.default_rng(3)
+    H = torch.from_numpy(rng.normal(0, 1, (5, 256)).astype(np.float32)).bfloat16().float().numpy()
+    Wr = torch.from_numpy(rng.normal(0, 0.05, (300, 256)).astype(np.float32)).bfloat16().float()
+    Wr = Wr.numpy()
+    got = orc.lmhead_logits(H, Wr)
+    ref = (H.astype(np.float64) @ Wr.astype(np.float64).T).astype(np.float32)
+    assert np.abs(got.astype(np.float64) - ref).max() <= 2 * np.abs(ref).max() * 2.0 ** -24

@@ -75,12 +75,6 @@ const char* sv_status_string(sv_status status);
 /* Library build identifier (static string), e.g. for logs. */
 const char* sv_version(void);
 
-/* Kernel timing (diagnostic, off by default).  While enabled on the calling host thread, every
- * spec_verify_token / spec_verify_block call records CUDA events on its stream around each of its
- * kernels: [0] row streaming (all passes), [1] acceptance decisions, [2] correction / bonus race.
- * sv_profile_read waits for the events of the last profiled call and returns the three durations
- * in milliseconds.  The events belong to the library (created on first use, one set per host
- * thread); nothing is recorded while profiling is disabled. */
 /* Failure-detection self test.  Runs one of the bounded device-side waits the kernels use on a
  * condition that never comes true -- which = 0: an mbarrier phase no thread completes; which = 1:
  * a shared-memory request-number word no thread publishes -- with a limit of `limit_us`
@@ -89,6 +83,13 @@ const char* sv_version(void);
  * context stays usable.  No page has a counterpart: it checks the library's own safety net. */
 sv_status sv_selftest_wait(int32_t which, int32_t limit_us, int32_t* status, void* stream);
 
+/* Kernel timing (diagnostic, off by default).  While enabled on the calling host thread, every
+ * spec_verify_token / spec_verify_block call records CUDA events on its stream around each of its
+ * kernels: [0] row streaming (all passes), [1] acceptance decisions, [2] correction / bonus race.
+ * sv_profile_read waits for the events of the last profiled call and returns the three durations
+ * in milliseconds.  The events belong to the library (created on first use, one set per host
+ * thread); nothing is recorded while profiling is disabled.  A spec_verify_lmhead call records
+ * [0] the statistics GEMM, [1] the decisions, [2] the race GEMM and the outputs. */
 sv_status sv_profile_enable(int enable);
 sv_status sv_profile_read(float* ms_out /* HOST [3] */);
 
@@ -239,6 +240,37 @@ sv_status spec_verify_shard_finish(const uint64_t* winners_all, int32_t n_shards
                                    const int32_t* draft_tokens, int32_t* out_tokens,
                                    int64_t out_ld, int32_t* correction_token, int32_t* status,
                                    void* stream);
+
+/* Token-level verification from hidden states ("How much does a token cost", "The Role of
+ * Arithmetic Intensity": a projection of Q input rows of width H by an [H, W] weight makes the
+ * Q x W logits).  The target's logit row i is target_hidden row i times W^T and the draft's logit
+ * row i is draft_hidden row i times W^T: the draft scores its tokens through the same output
+ * projection as the target.  The logits are computed on the tensor cores (bf16 products, fp32
+ * sums) and folded as they are produced; none is written to memory.  Given those logits the call
+ * decides and samples exactly as spec_verify_token does on stored logits (same Philox streams,
+ * same outputs, same data-error reporting), the logits being the fp32 sums rather than stored
+ * values.
+ *   target_hidden / draft_hidden  DEVICE bf16, row stride ldh elements (multiple of 8, >= H); the
+ *                                 rows of request r are target_row0[r] + 0 .. gamma_r and
+ *                                 draft_row0[r] + 0 .. gamma_r - 1, as for the logit rows of
+ *                                 spec_verify_token.
+ *   W                             DEVICE bf16 [V][ldw] (ldw multiple of 8, >= H): row v is token
+ *                                 v's output vector.
+ *   H                             hidden size, a multiple of 64.
+ * All DEVICE pointers 16-byte aligned; SV_ERR_UNSUPPORTED otherwise, or for V above 2^31 - 256.
+ * The workspace (DEVICE, 256-byte aligned) holds a copy of the hidden rows in GEMM order and the
+ * per-tile partials: spec_verify_lmhead_workspace_bytes(B, max_draft_len, V, H) bytes, 0 for sizes
+ * the call rejects. */
+size_t spec_verify_lmhead_workspace_bytes(int32_t B, int32_t max_draft_len, int64_t V, int64_t H);
+sv_status spec_verify_lmhead(const void* target_hidden, const void* draft_hidden, int64_t ldh,
+                             const void* W, int64_t ldw, int64_t H, int64_t V,
+                             const int64_t* target_row0, const int64_t* draft_row0,
+                             const int32_t* draft_len, int32_t max_draft_len,
+                             const int32_t* draft_tokens, int32_t B, uint64_t seed,
+                             const uint64_t* request_ids, int32_t* accepted_len,
+                             int32_t* out_tokens, int64_t out_ld, int32_t* correction_token,
+                             float* accept_ratio, int32_t* status, void* workspace,
+                             size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * DSpark draft side.

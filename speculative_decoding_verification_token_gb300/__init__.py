@@ -77,6 +77,9 @@ def lib():
             "spec_verify_shard_race": (st, [P, P, st, i64, i64, i64, i64, P, P, P, i32, P, i32,
                                             u64, P, P, P, P, P, P, P, P, sz, P]),
             "spec_verify_shard_finish": (st, [P, i32, i32, P, P, P, P, i64, P, P, P]),
+            "spec_verify_lmhead_workspace_bytes": (sz, [i32, i32, i64, i64]),
+            "spec_verify_lmhead": (st, [P, P, i64, P, i64, i64, i64, P, P, P, i32, P, i32, u64,
+                                        P, P, P, i64, P, P, P, P, sz, P]),
             "dspark_schedule_rule": (st, [P, P, i32, i32, P, i32, i32, P, P, P, P, P, P, sz, P]),
             "dspark_schedule_async": (st, [P, i32, i64, P, P, i32, i32, P, i32, i32, P, P, P, P, P,
                                            P, sz, P]),
@@ -239,6 +242,51 @@ def spec_verify_block(target, draft, target_row0, draft_row0, draft_len, max_dra
     """Block verification (see include/specverify.h).  Returns a dict of device tensors."""
     return _verify(True, target, draft, target_row0, draft_row0, draft_len, max_draft_len,
                    draft_tokens, seed, request_ids, out_ld, want_rows, status, workspace, stream)
+
+
+def spec_verify_lmhead_workspace_bytes(B, max_draft_len, V, H):
+    return int(lib().spec_verify_lmhead_workspace_bytes(B, max_draft_len, V, H))
+
+
+def spec_verify_lmhead(target_hidden, draft_hidden, W, target_row0, draft_row0, draft_len,
+                       max_draft_len, draft_tokens, seed, request_ids=None, out_ld=None,
+                       want_ratio=True, status=None, workspace=None, stream=None):
+    """Token-level verification from hidden states: logits = hidden rows x W^T (bf16 operands,
+    W [V, H]), decided and sampled as spec_verify_token does (see include/specverify.h).
+    Returns a dict of device tensors."""
+    _dev(target_hidden, torch.bfloat16, rows=True), _dev(draft_hidden, torch.bfloat16, rows=True)
+    _dev(W, torch.bfloat16, rows=True)
+    _dev(target_row0, torch.int64), _dev(draft_row0, torch.int64)
+    _dev(draft_len, torch.int32), _dev(draft_tokens, torch.int32)
+    _dev(request_ids)
+    H = target_hidden.shape[-1]
+    if draft_hidden.shape[-1] != H or W.shape[-1] != H:
+        raise ValueError("hidden rows and W must have the same width H")
+    ldh = target_hidden.stride(0)
+    if draft_hidden.stride(0) != ldh:
+        raise ValueError("target and draft hidden rows must have the same stride")
+    V = W.shape[0]
+    B = draft_len.numel()
+    out_ld = out_ld or max_draft_len + 1
+    dev = target_hidden.device
+    accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    out_tokens = torch.empty((B, out_ld), dtype=torch.int32, device=dev)
+    correction = torch.empty(B, dtype=torch.int32, device=dev)
+    ratio = (torch.empty(draft_tokens.numel(), dtype=torch.float32, device=dev)
+             if want_ratio else None)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    need = spec_verify_lmhead_workspace_bytes(B, max_draft_len, V, H)
+    ws = workspace if workspace is not None else globals()["workspace"](need, dev)
+    code = lib().spec_verify_lmhead(_ptr(target_hidden), _ptr(draft_hidden), ldh, _ptr(W),
+                                    W.stride(0), H, V, _ptr(target_row0), _ptr(draft_row0),
+                                    _ptr(draft_len), int(max_draft_len), _ptr(draft_tokens), B,
+                                    int(seed), _ptr(request_ids), _ptr(accepted),
+                                    _ptr(out_tokens), out_ld, _ptr(correction), _ptr(ratio),
+                                    _ptr(status), _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "spec_verify_lmhead")
+    return {"accepted_len": accepted, "out_tokens": out_tokens, "correction": correction,
+            "accept_ratio": ratio, "status": status}
 
 
 def spec_sample_draft(draft, draft_row0, draft_len, max_draft_len, seed, request_ids=None,

@@ -86,33 +86,6 @@ __global__ void shard_merge_kernel(const float4* stats_all, const float2* tok_al
   tok_out[u] = tk;
 }
 
-// The largest winner over the shards -- the race over p's if no shard had a residual entry -- and
-// the request's outputs.  One thread per request.
-__global__ void shard_finish_kernel(const unsigned long long* winners_all, int32_t n, int32_t B,
-                                    const int32_t* accepted_len, const int64_t* draft_row0,
-                                    const int32_t* draft_tokens, int32_t* out_tokens,
-                                    int64_t out_ld, int32_t* correction_token, int32_t* status) {
-  const int32_t r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= B) return;
-  unsigned long long best = 0ull, fb = 0ull;
-  for (int32_t k = 0; k < n; ++k) {
-    best = max(best, winners_all[(size_t(k) * B + r) * 2]);
-    fb = max(fb, winners_all[(size_t(k) * B + r) * 2 + 1]);
-  }
-  if (!best) best = fb;
-  const int32_t y = best ? race_unpack_index(best) : -1;
-  if (y < 0) report(status, SV_ERR_BAD_INPUT);  // the row carries no probability at all
-  const int32_t tau = accepted_len[r];
-  int32_t* out = out_tokens + size_t(r) * out_ld;
-  for (int64_t q = 0; q < out_ld; ++q) {
-    int32_t v = -1;
-    if (q < tau) v = draft_tokens[draft_row0[r] + q];
-    else if (q == tau) v = y;
-    out[q] = v;
-  }
-  if (correction_token) correction_token[r] = y;
-}
-
 bool shard_args_ok(const CommonArgs& a, int64_t v_off, int64_t V_total) {
   return v_off >= 0 && v_off % 8 == 0 && V_total >= v_off + a.V && V_total < (int64_t(1) << 31);
 }
@@ -311,7 +284,7 @@ extern "C" sv_status spec_verify_shard_finish(const uint64_t* winners_all, int32
   if (!winners_all || !accepted_len || !out_tokens) return SV_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (status && cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return SV_ERR_CUDA;
-  shard_finish_kernel<<<unsigned((B + 127) / 128), 128, 0, s>>>(
+  winners_finish_kernel<<<unsigned((B + 127) / 128), 128, 0, s>>>(
       reinterpret_cast<const unsigned long long*>(winners_all), n_shards, B, accepted_len,
       draft_row0, draft_tokens, out_tokens, out_ld, correction_token, status);
   return launch_status(cudaGetLastError());

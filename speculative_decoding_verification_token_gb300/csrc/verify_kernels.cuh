@@ -18,7 +18,9 @@
 //           64-bit atomic max per request and the last share to finish writes the outputs.  It is
 //           launched as a programmatic dependent of the kernel before it, so its launch overlaps
 //           that kernel's tail.
-// Everything here has internal linkage: each of the two files compiles its own copy.
+//   finish  the partial race winners of a request folded into its outputs (vocabulary shards,
+//           and the tiles of the race over recomputed logits in lmhead.cu).
+// Everything here has internal linkage: each file that includes it compiles its own copy.
 #pragma once
 
 #include "verify_common.cuh"
@@ -649,6 +651,40 @@ static sv_status launch_race(RaceParams rp, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return launch_status(cudaLaunchKernelEx(&cfg, race_kernel<E, kBlock>, rp));
+}
+
+// ---------------------------------------------------------------------------------------------
+// finish: partial race winners -> outputs
+// ---------------------------------------------------------------------------------------------
+// The largest of n partial race winners per request -- the largest of the race over p if no
+// partial had a residual entry -- and the request's outputs.  winners_all is [n][B][2] packed
+// results (race_pack; 0: none), the residual (or bonus) winner first, the race over p second.
+// One thread per request.
+template <int kDummy = 0>
+__global__ void winners_finish_kernel(const unsigned long long* winners_all, int32_t n,
+                                      int32_t B, const int32_t* accepted_len,
+                                      const int64_t* draft_row0, const int32_t* draft_tokens,
+                                      int32_t* out_tokens, int64_t out_ld,
+                                      int32_t* correction_token, int32_t* status) {
+  const int32_t r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= B) return;
+  unsigned long long best = 0ull, fb = 0ull;
+  for (int32_t k = 0; k < n; ++k) {
+    best = max(best, winners_all[(size_t(k) * B + r) * 2]);
+    fb = max(fb, winners_all[(size_t(k) * B + r) * 2 + 1]);
+  }
+  if (!best) best = fb;
+  const int32_t y = best ? race_unpack_index(best) : -1;
+  if (y < 0) report(status, SV_ERR_BAD_INPUT);  // the row carries no probability at all
+  const int32_t tau = accepted_len[r];
+  int32_t* out = out_tokens + size_t(r) * out_ld;
+  for (int64_t q = 0; q < out_ld; ++q) {
+    int32_t v = -1;
+    if (q < tau) v = draft_tokens[draft_row0[r] + q];
+    else if (q == tau) v = y;
+    out[q] = v;
+  }
+  if (correction_token) correction_token[r] = y;
 }
 
 }  // namespace

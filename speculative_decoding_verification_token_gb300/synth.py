@@ -15,6 +15,8 @@ Workloads (logits are row-major, one row per (request, position)):
 * ``markov``       -- 256 requests, block length 16, V = 151936; backbone logits N(0, 2^2) bf16;
   U [V, 256] and W [256, V] bf16 N(0, 0.02^2); anchors uniform over the vocabulary; confidence
   scores N(0, 1); per-position STS temperatures U[0.8, 1.2].
+* ``lmhead``       -- 64 requests, 5 drafted positions, V = 151936, hidden size 2560; bf16 hidden
+  rows and output projection whose products give the ``token_large`` logit recipe.
 * ``scheduled``    -- 512 requests x 16 positions; conditional acceptance c[i, k] = Beta(8, 2) draw
   times 0.97^(k-1); engine curve SPS(B) = 1 / (2 ms + B * 0.4 us) for B <= 8192; logits for all 17
   target and 16 draft rows per request as in ``token_large`` with V = 129280.
@@ -155,6 +157,70 @@ def markov_inputs(w: MarkovWorkload, device="cpu"):
         "scores": scores.float(),
         "T": T.float(),
         "B": B, "K": K, "V": V, "R": R,
+        "seed": w.seed,
+    }
+
+
+@dataclass(frozen=True)
+class LmHeadWorkload:
+    name: str
+    B: int
+    gamma: int
+    V: int
+    H: int
+    target_std: float      # std of the target logits h . W[v] (before the prior)
+    zipf: float            # exponent of the log-prior over token ids, carried by hidden column 0
+    draft_noise: float     # std of the draft logits' deviation from the target's
+    seed: int
+    gen_seed: int
+
+
+# Verification from hidden states: 64 requests, 5 drafted positions, V = 151936, hidden size 2560
+# (a Qwen3-4B-sized target), bf16.  Logits h . W[v] ~ N(0, 3^2) plus the Zipf(1.1) prior, draft
+# logits = target + N(0, 1): the token_large logit recipe, produced through an output projection.
+LMHEAD = LmHeadWorkload("lmhead", 64, 5, 151936, 2560, 3.0, 1.1, 1.0, 6, 1007)
+# Parity case: several slot blocks and vocabulary tiles with ragged tails (V % 256 != 0), and an
+# odd number of 64-wide k-blocks.
+LMHEAD_SMALL = LmHeadWorkload("lmhead_small", 24, 5, 4099, 320, 3.0, 1.1, 1.0, 7, 1008)
+
+
+def lmhead_inputs(w: LmHeadWorkload, device="cpu", draft_len=None):
+    """Hidden rows and the output projection of a verify-from-hidden-states workload.
+
+    Target hidden rows h ~ N(0, 1) and W ~ N(0, (target_std / sqrt(H - 1))^2) make h . W[v] ~
+    N(0, target_std^2); hidden column 0 is the constant 1 and W[v][0] = -zipf ln(v + 1), so every
+    logit carries the prior.  Draft row j of a request is its target row j plus
+    N(0, (draft_noise / target_std)^2) in columns 1.., so draft logits = target + N(0,
+    draft_noise^2).  Row layout as in token_inputs: request r owns target rows r (gamma + 1) + j and
+    draft rows r gamma + j.
+    """
+    B, G, V, H = w.B, w.gamma, w.V, w.H
+    g = _gen(device, w.gen_seed)
+    n_t, n_d = B * (G + 1), B * G
+    target = torch.randn((n_t, H), generator=g, device=device, dtype=torch.float32)
+    W = torch.randn((V, H), generator=g, device=device, dtype=torch.float32)
+    W.mul_(w.target_std / math.sqrt(H - 1))
+    target[:, 0] = 1.0
+    W[:, 0] = -w.zipf * torch.log(torch.arange(V, device=device, dtype=torch.float32) + 1.0)
+    t_view = target.view(B, G + 1, H)[:, :G, :].reshape(n_d, H)
+    noise = torch.randn((n_d, H), generator=g, device=device, dtype=torch.float32)
+    noise.mul_(w.draft_noise / w.target_std)
+    noise[:, 0] = 0.0
+    draft = t_view + noise
+    if draft_len is None:
+        draft_len = torch.full((B,), G, dtype=torch.int32)
+    draft_len = torch.as_tensor(draft_len, dtype=torch.int32).to(device)
+    return {
+        "target_hidden": target.to(torch.bfloat16),
+        "draft_hidden": draft.to(torch.bfloat16),
+        "W": W.to(torch.bfloat16),
+        "V": V,
+        "H": H,
+        "target_row0": (torch.arange(B, dtype=torch.int64) * (G + 1)).to(device),
+        "draft_row0": (torch.arange(B, dtype=torch.int64) * G).to(device),
+        "draft_len": draft_len,
+        "max_draft_len": G,
+        "B": B,
         "seed": w.seed,
     }
 

@@ -257,6 +257,13 @@ sv_status spec_verify_shard_finish(const uint64_t* winners_all, int32_t n_shards
  *   W                             DEVICE bf16 [V][ldw] (ldw multiple of 8, >= H): row v is token
  *                                 v's output vector.
  *   H                             hidden size, a multiple of 64.
+ *   recomputed                    DEVICE [1] (nullable): how many requests' correction tokens
+ *                                 needed the second pass (below); the rest were settled by the
+ *                                 candidates the first pass kept.
+ * Two passes over W at most.  The first computes every logit once: the softmax statistics and,
+ * per position, the few entries that can win the correction or bonus race; the second recomputes
+ * the two rows of only those requests whose candidates cannot prove their winner, and is skipped
+ * (an empty launch) when there are none.  The outputs do not depend on which pass settled them.
  * All DEVICE pointers 16-byte aligned; SV_ERR_UNSUPPORTED otherwise, or for V above 2^31 - 256.
  * The workspace (DEVICE, 256-byte aligned) holds a copy of the hidden rows in GEMM order and the
  * per-tile partials: spec_verify_lmhead_workspace_bytes(B, max_draft_len, V, H) bytes, 0 for sizes
@@ -269,8 +276,8 @@ sv_status spec_verify_lmhead(const void* target_hidden, const void* draft_hidden
                              const int32_t* draft_tokens, int32_t B, uint64_t seed,
                              const uint64_t* request_ids, int32_t* accepted_len,
                              int32_t* out_tokens, int64_t out_ld, int32_t* correction_token,
-                             float* accept_ratio, int32_t* status, void* workspace,
-                             size_t workspace_bytes, void* stream);
+                             float* accept_ratio, int32_t* recomputed, int32_t* status,
+                             void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * DSpark draft side.

@@ -79,7 +79,7 @@ def lib():
             "spec_verify_shard_finish": (st, [P, i32, i32, P, P, P, P, i64, P, P, P]),
             "spec_verify_lmhead_workspace_bytes": (sz, [i32, i32, i64, i64]),
             "spec_verify_lmhead": (st, [P, P, i64, P, i64, i64, i64, P, P, P, i32, P, i32, u64,
-                                        P, P, P, i64, P, P, P, P, sz, P]),
+                                        P, P, P, i64, P, P, P, P, P, sz, P]),
             "dspark_schedule_rule": (st, [P, P, i32, i32, P, i32, i32, P, P, P, P, P, P, sz, P]),
             "dspark_schedule_async": (st, [P, i32, i64, P, P, i32, i32, P, i32, i32, P, P, P, P, P,
                                            P, sz, P]),
@@ -274,6 +274,7 @@ def spec_verify_lmhead(target_hidden, draft_hidden, W, target_row0, draft_row0, 
     correction = torch.empty(B, dtype=torch.int32, device=dev)
     ratio = (torch.empty(draft_tokens.numel(), dtype=torch.float32, device=dev)
              if want_ratio else None)
+    recomputed = torch.zeros(1, dtype=torch.int32, device=dev)
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
     need = spec_verify_lmhead_workspace_bytes(B, max_draft_len, V, H)
@@ -283,10 +284,11 @@ def spec_verify_lmhead(target_hidden, draft_hidden, W, target_row0, draft_row0, 
                                     _ptr(draft_len), int(max_draft_len), _ptr(draft_tokens), B,
                                     int(seed), _ptr(request_ids), _ptr(accepted),
                                     _ptr(out_tokens), out_ld, _ptr(correction), _ptr(ratio),
-                                    _ptr(status), _ptr(ws), ws.numel(), _stream(stream))
+                                    _ptr(recomputed), _ptr(status), _ptr(ws), ws.numel(),
+                                    _stream(stream))
     _check(code, "spec_verify_lmhead")
     return {"accepted_len": accepted, "out_tokens": out_tokens, "correction": correction,
-            "accept_ratio": ratio, "status": status}
+            "accept_ratio": ratio, "recomputed": recomputed, "status": status}
 
 
 def spec_sample_draft(draft, draft_row0, draft_len, max_draft_len, seed, request_ids=None,

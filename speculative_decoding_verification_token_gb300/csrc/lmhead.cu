@@ -3,7 +3,7 @@
 // The target's and the draft's logits are the products of their hidden states with one output
 // projection W [V][H] ("How much does a token cost", "The Role of Arithmetic Intensity": inputs
 // [Q, H] times weights [H, W]).  They are computed on the tensor cores and folded as they leave
-// the accumulators; no logit is ever written to memory.  Five kernels on the caller's stream:
+// the accumulators; no logit is ever written to memory.  Kernels on the caller's stream:
 //   gather  the hidden rows of every request into the GEMM's A operand, two slots per position:
 //           slot 2j holds target row j, slot 2j + 1 draft row j, 2 (gmax + 1) slots per request
 //           (the slots a request does not use are never read back);
@@ -14,17 +14,25 @@
 //                         accumulators;
 //             warps 2-17  the epilogue, a lane quadrant (32 slots) and a column quarter each: the
 //                         log2-domain softmax statistics of every slot and the drafted token's
-//                         logit; one (m_t, s_t, m_d, s_d) partial per (row pair, CTA);
+//                         logit -- one (m_t, s_t, m_d, s_d) partial per (row pair, CTA) -- and the
+//                         race candidates of every position: each target slot and its draft slot
+//                         (neighbouring lanes) split the columns and keep the kLmCand entries of
+//                         largest plain key a = t - log E (E the entry's exponential variable of
+//                         the position's correction or bonus stream), with d - t beside each;
 //   decide  one CTA per request: the row normalisers, p(x)/q(x), the ACCEPT uniforms and the first
-//           rejection, exactly as token-level verification of stored logits decides; it copies the
-//           two hidden rows the race needs (target and draft row of the rejected position, or the
-//           target row of the bonus position) into a second A operand;
-//   race    the same GEMM over those rows (128-column tiles); the epilogue pairs each target slot
-//           with its draft slot and runs the exponential race of the correction (or bonus) token
-//           on the recomputed logits, gated against a bound every CTA of the request publishes;
-//   finish  the partial winners of every request folded into its outputs.
-// The statistics of a row need every column before any residual weight is known, so the race's
-// two rows are recomputed rather than kept: W is read twice, and the logits never reach memory.
+//           rejection, exactly as token-level verification of stored logits decides; then the race
+//           over the candidates of the rejected (or bonus) position.  Every entry a lane did not
+//           keep has a plain key no larger than that lane's bound theta (its last kept key, or the
+//           gate key shared by all lanes of the position that it was dropped against), and its
+//           residual key a + log(1 - exp(d - t + gap)) is smaller still; so the candidates' winner
+//           is the race's winner whenever its key exceeds every theta (always, for a bonus token).
+//           Otherwise the request is queued and its two hidden rows are copied into a second A
+//           operand;
+//   race    the same GEMM over the queued requests' rows (128-column tiles; no work and an early
+//           exit when the queue is empty): the epilogue pairs each target slot with its draft slot
+//           and runs the exponential race on the recomputed logits, gated against a bound every
+//           CTA of the request publishes;
+//   finish  the outputs: the candidates' winner, or the folded partial winners of a queued request.
 #include <algorithm>
 
 #include "tc.cuh"
@@ -41,6 +49,9 @@ constexpr uint32_t kLmABytes = kLmRows * 128;  // one 64-element k-block of the 
 constexpr uint32_t kLmRingBytes = 196608;      // the operand ring
 constexpr int kLmStatsN = 256;                 // vocabulary columns per tile, statistics GEMM
 constexpr int kLmRaceN = 128;                  // the same, race GEMM
+constexpr int kLmCand = 8;                     // race candidates kept per lane and position
+constexpr int kLmParts = 8;                    // candidate partitions per (position, CTA):
+                                               // 4 column quarters x 2 lanes of a slot pair
 
 template <int kN>
 struct LmShape {
@@ -63,12 +74,17 @@ struct LmParams {
   const int32_t* draft_tokens;
   float4* partials;  // [B * gmax][per_mblock]: (m_t, s_t, m_d, s_d), log2 domain
   float2* tok;       // [B * gmax]: the drafted token's target and draft logits
+  float4* cand;      // [B (gmax + 1)][per_mblock][kLmParts][kLmCand]: (a, d - t, index, 0)
+  float* theta;      // [B (gmax + 1)][per_mblock][kLmParts]: bound on the dropped entries' a
+  uint32_t* cpub;    // [B (gmax + 1)] largest last-kept key any lane has published (key_order)
   // race
   const RaceDesc* desc;          // [B]
   uint64_t seed;
   const uint64_t* request_ids;
   uint32_t* k0;                  // [B] best exact race key published so far (key_order; 0: none)
   unsigned long long* winners;   // [per_mblock][B][2] packed partial winners
+  const int32_t* race_count;     // requests queued for the race GEMM
+  const int32_t* race_list;      // [B] the queued requests, in queue order
   int32_t* status;
 };
 
@@ -81,15 +97,21 @@ __device__ __forceinline__ void copy_row(uint8_t* dst, const uint8_t* src, int64
 }
 
 // Slot block of the statistics GEMM: request r's target row j into slot r S + 2j (j <= g), its
-// draft row j into slot r S + 2j + 1 (j < g).  One CTA per request; block 0 clears the status.
+// draft row j into slot r S + 2j + 1 (j < g).  One CTA per request, which also clears the
+// request's published candidate bounds; block 0 clears the status and the race queue.
 __global__ void __launch_bounds__(256)
     lm_gather_kernel(const uint8_t* __restrict__ th, const uint8_t* __restrict__ dh, int64_t ldh,
                      int64_t H, const int64_t* __restrict__ target_row0,
                      const int64_t* __restrict__ draft_row0, const int32_t* __restrict__ draft_len,
-                     int32_t gmax, uint8_t* __restrict__ A, int32_t* status) {
+                     int32_t gmax, uint8_t* __restrict__ A, uint32_t* cpub,
+                     int32_t* race_count, int32_t* status) {
   const int32_t r = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (r == 0 && threadIdx.x == 0 && status) *status = 0;
+  if (r == 0 && threadIdx.x == 0) {
+    *race_count = 0;
+    if (status) *status = 0;
+  }
+  for (int32_t j = threadIdx.x; j <= gmax; j += blockDim.x) cpub[size_t(r) * (gmax + 1) + j] = 0u;
   const int32_t g = clamp_gamma(draft_len[r], gmax);
   const int32_t S = 2 * (gmax + 1);
   const int64_t row_bytes = H * 2;
@@ -99,38 +121,6 @@ __global__ void __launch_bounds__(256)
                                  : th + (target_row0[r] + j) * ldh * 2;
     copy_row(A + (int64_t(r) * S + s) * row_bytes, src, row_bytes, lane);
   }
-}
-
-// The decision of request r (decide_body, on the statistics partials and the drafted tokens'
-// logits the statistics GEMM left), then the race rows: slot 2r <- target row tau, slot 2r + 1 <-
-// draft row tau (residual) -- both already in the statistics slot block.
-struct LmDecideParams {
-  DecideParams dp;
-  const uint8_t* A1;
-  uint8_t* A2;
-  int64_t row_bytes;
-  RaceDesc* desc;
-  uint32_t* k0;
-  int32_t* accepted_len;
-};
-
-__global__ void __launch_bounds__(kThreads) lm_decide_kernel(LmDecideParams p) {
-  __shared__ RaceDesc s_desc;
-  __shared__ int32_t s_tok[SV_MAX_DRAFT_LEN];
-  const int32_t r = blockIdx.x;
-  decide_body<float>(p.dp, r, true, &s_desc, s_tok, false);
-  __syncthreads();
-  const RaceDesc d = s_desc;
-  if (threadIdx.x == 0) {
-    p.desc[r] = d;
-    p.k0[r] = 0u;
-    p.accepted_len[r] = d.tau;
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int32_t S = 2 * (p.dp.gmax + 1);
-  if (warp < (d.resid ? 2 : 1))
-    copy_row(p.A2 + (int64_t(2) * r + warp) * p.row_bytes,
-             p.A1 + (int64_t(r) * S + 2 * d.tau + warp) * p.row_bytes, p.row_bytes, lane);
 }
 
 struct KeyIdx {
@@ -155,6 +145,149 @@ __device__ __forceinline__ void key_entry(const RaceSpec& rs, float t, float d, 
   if (race_active(rs, t, d)) offer_key(race_key(rs, t, d, noise), e, best);
 }
 
+// ---- race candidates: per lane, the kLmCand entries of largest plain key a = t - log E seen so
+// far (unordered), with the position and key of the smallest.  The keys stay in registers; each
+// entry's b = d - t and index sit in shared memory (bx[i * kBxStride], this lane's column of the
+// block's candidate buffer), written only when an entry enters the list.  Equal keys may be kept
+// either way: the decision only needs every dropped entry's key to be no larger than a bound.
+constexpr int kBxStride = 32 * kLmEpiWarps;
+
+struct CandList {
+  float a[kLmCand];
+  float amin;  // smallest kept key (-inf while the list is not full)
+  int pmin;    // its position
+  float2* bx;  // (b, index as float bits) of entry i at bx[i * kBxStride]
+};
+
+__device__ __forceinline__ void cand_init(CandList& c, float2* bx) {
+  c.bx = bx;
+#pragma unroll
+  for (int i = 0; i < kLmCand; ++i) {
+    c.a[i] = -INFINITY;
+    c.bx[i * kBxStride] = make_float2(0.f, __int_as_float(-1));
+  }
+  c.amin = -INFINITY;
+  c.pmin = 0;
+}
+
+// (a, b, e) replaces the smallest entry (the caller checked a > amin).
+__device__ __forceinline__ void cand_insert(CandList& c, float a, float b, int32_t e) {
+  c.bx[c.pmin * kBxStride] = make_float2(b, __int_as_float(e));
+#pragma unroll
+  for (int i = 0; i < kLmCand; ++i)
+    if (i == c.pmin) c.a[i] = a;
+  float m = c.a[0];
+  int pm = 0;
+#pragma unroll
+  for (int i = 1; i < kLmCand; ++i)
+    if (c.a[i] < m) {
+      m = c.a[i];
+      pm = i;
+    }
+  c.amin = m;
+  c.pmin = pm;
+}
+
+// Offers 16 entries (columns e0 .. e0 + 15, e0 a multiple of 16) with target logits tt and draft
+// logits dd, against the gate key G: an entry enters the list only if its plain key exceeds both
+// the list's smallest key and G.  Its logit must then be within kMaxNoise of that bound, and its
+// Philox word must pass the noise gate of race.cuh; the few entries that pass are keyed exactly.
+__device__ __forceinline__ void cand_offer16(CandList& c, const Stream& st, const float* tt,
+                                             const float* dd, int64_t e0, float G) {
+#pragma unroll
+  for (int g4 = 0; g4 < 4; ++g4) {
+    const float T = fmaxf(c.amin, G);
+    const float tm = fmaxf(fmaxf(tt[4 * g4], tt[4 * g4 + 1]), fmaxf(tt[4 * g4 + 2], tt[4 * g4 + 3]));
+    if (!(tm >= T - kMaxNoise)) continue;
+    const float cg = 23.0f - T * kLog2e;
+    const uint4 blk = stream_block(st, static_cast<uint32_t>((e0 >> 2) + g4));
+    const uint32_t w4[4] = {blk.x, blk.y, blk.z, blk.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float t = tt[4 * g4 + q];
+      if (!(t > -INFINITY) || !(gate_m(w4[q]) <= gate_threshold(t, cg))) continue;
+      const float a = t + race_noise(uniform_of(w4[q]));
+      if (a > c.amin && a > G)
+        cand_insert(c, a, dd[4 * g4 + q] - t, static_cast<int32_t>(e0 + 4 * g4 + q));
+    }
+  }
+}
+
+// The decision of request r (decide_body, on the statistics partials and the drafted tokens'
+// logits the statistics GEMM left), then the race over the candidates of its correction (or
+// bonus) position; a request the candidates cannot settle is queued for the race GEMM with its
+// two rows: queue slot i <- target row tau (slot 2i) and draft row tau (slot 2i + 1), both copied
+// from the statistics slot block.
+struct LmDecideParams {
+  DecideParams dp;
+  const uint8_t* A1;
+  uint8_t* A2;
+  int64_t row_bytes;
+  RaceDesc* desc;
+  uint32_t* k0;
+  int32_t* accepted_len;
+  const float4* cand;
+  const float* theta;
+  int32_t C;                      // statistics CTAs per slot block
+  unsigned long long* decided;    // [B] packed winner of a settled request
+  int32_t* pending;               // [B] 1: queued for the race GEMM
+  int32_t* race_count;
+  int32_t* race_list;
+};
+
+__global__ void __launch_bounds__(kThreads) lm_decide_kernel(LmDecideParams p) {
+  __shared__ RaceDesc s_desc;
+  __shared__ int32_t s_tok[SV_MAX_DRAFT_LEN];
+  __shared__ float red_k[kWarps];
+  __shared__ int32_t red_i[kWarps];
+  __shared__ int32_t s_slot;
+  const int32_t r = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  decide_body<float>(p.dp, r, true, &s_desc, s_tok, false);
+  __syncthreads();
+  const RaceDesc d = s_desc;
+  const size_t u2 = size_t(r) * (p.dp.gmax + 1) + d.tau;
+  const int32_t n_parts = p.C * kLmParts;
+  const float4* cd = p.cand + u2 * n_parts * kLmCand;
+  KeyIdx best = {-INFINITY, -1};
+  for (int32_t i = tid; i < n_parts * kLmCand; i += kThreads) {
+    const float4 q = cd[i];
+    const int32_t e = __float_as_int(q.z);
+    if (e < 0) continue;
+    if (!d.resid) {
+      offer_key(q.x, e, best);
+    } else {
+      const float y = q.y + d.gap;
+      if (y < 0.f) offer_key(q.x + __logf(one_minus_exp(y)), e, best);
+    }
+  }
+  float bound = -INFINITY;  // largest plain key an unkept entry may have
+  for (int32_t i = tid; i < n_parts; i += kThreads) bound = fmaxf(bound, p.theta[u2 * n_parts + i]);
+  block_race<kThreads>(best.key, best.idx, red_k, red_i);
+  bound = block_max<kThreads>(bound, red_k);
+  // settled: a bonus (its winner has the largest plain key of all, which some partition kept), or
+  // a residual winner above every unkept entry's plain key
+  const bool settled = !d.resid || (best.idx >= 0 && best.key > bound);
+  if (tid == 0) {
+    p.desc[r] = d;
+    p.accepted_len[r] = d.tau;
+    p.pending[r] = settled ? 0 : 1;
+    p.decided[r] = (settled && best.idx >= 0) ? race_pack(best.key, best.idx) : 0ull;
+    if (!settled) {
+      p.k0[r] = 0u;
+      const int32_t i = atomicAdd(p.race_count, 1);
+      p.race_list[i] = r;
+      s_slot = i;
+    }
+  }
+  __syncthreads();
+  if (settled) return;
+  const int32_t S = 2 * (p.dp.gmax + 1);
+  if (warp < (d.resid ? 2 : 1))
+    copy_row(p.A2 + (int64_t(2) * s_slot + warp) * p.row_bytes,
+             p.A1 + (int64_t(r) * S + 2 * d.tau + warp) * p.row_bytes, p.row_bytes, lane);
+}
+
 template <int kN, bool kRace>
 __global__ void __launch_bounds__(kLmThreads, 1)
     lm_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -168,13 +301,22 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   __shared__ uint64_t full[kStages], empty[kStages];
   __shared__ uint64_t acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base;
-  __shared__ float4 merge[3][kLmRows];  // column quarters 1..3 -> quarter 0
+  // the epilogue's candidate buffer ([kLmCand][kBxStride] float2), reused afterwards for the
+  // merge of column quarters 1..3 into quarter 0 ([3][kLmRows] float4)
+  __shared__ __align__(16) uint8_t epi_buf[kLmCand * kBxStride * sizeof(float2)];
+  static_assert(sizeof(epi_buf) >= 3 * kLmRows * sizeof(float4), "merge area");
+  float4 (*merge)[kLmRows] = reinterpret_cast<float4 (*)[kLmRows]>(epi_buf);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t mb = blockIdx.x % p.n_mblocks;
   const int32_t ci = blockIdx.x / p.n_mblocks;
   const int32_t m0 = mb * kLmRows;
   const int32_t n_my = ci < p.n_tiles ? (p.n_tiles - ci + p.per_mblock - 1) / p.per_mblock : 0;
+  int32_t queued = 0;  // race GEMM: requests in the queue (two slots each)
+  if constexpr (kRace) {
+    queued = *reinterpret_cast<const volatile int32_t*>(p.race_count);
+    if (m0 >= 2 * queued) return;  // the whole CTA: nothing allocated or initialised yet
+  }
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -252,18 +394,37 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const int h = (warp - 2) >> 2;
     const uint32_t rl = 32 * q + lane;
     const int32_t R = m0 + static_cast<int32_t>(rl);
-    const int32_t r = R / p.slots;
     const int32_t kind = R & 1;  // 0: target slot, 1: draft slot
-    const bool row_ok = r < p.B;
     bool failed = false;
 
     if constexpr (!kRace) {
+      const int32_t r = R / p.slots;
+      const bool row_ok = r < p.B;
       const int32_t j = (R - r * p.slots) >> 1;  // 0-based position of the row pair
       int32_t x = -1;                            // drafted token of the pair, if any
+      int32_t mode = 0;                          // 1: correction candidates, 2: bonus candidates
+      uint64_t req = 0;
       if (row_ok) {
         const int32_t g = clamp_gamma(p.draft_len[r], p.gmax);
-        if (j < g) x = p.draft_tokens[p.draft_row0[r] + j];
+        if (j < g) {
+          x = p.draft_tokens[p.draft_row0[r] + j];
+          mode = 1;
+        } else if (j == g) {
+          mode = 2;
+        }
+        req = p.request_ids ? p.request_ids[r] : uint64_t(r);
       }
+      const Stream st = make_stream(p.seed, req, static_cast<uint32_t>(j + 1),
+                                    mode == 1 ? kTagResid : kTagBonus);
+      // Candidate gate shared by every lane of the position (all CTAs): the largest last-kept key
+      // any full list has published.  An entry below it is not needed from this lane either: its
+      // plain key is no larger than that lane's bound, which the decision checks anyway.
+      uint32_t* const cslot = mode ? p.cpub + size_t(r) * (p.gmax + 1) + j : nullptr;
+      float G = -INFINITY;          // gate key read at the previous tile
+      float gate_max = -INFINITY;   // largest gate key used
+      float published = -INFINITY;  // the largest key this lane has published
+      CandList cl;
+      cand_init(cl, reinterpret_cast<float2*>(epi_buf) + (tid - 64));
       float m2 = kM2Empty, sum = 0.f, xl = 0.f;
       float xf = 0.f;  // 1: this CTA saw the drafted token's column
       for (int t = 0; t < n_my; ++t) {
@@ -272,47 +433,85 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         if (!failed && !mbar_wait(&acc_full[acc], (t >> 1) & 1, p.status)) failed = true;
         __syncwarp();
         tc::fence_after_sync();
-        float v[kCols];
+        gate_max = fmaxf(gate_max, G);
 #pragma unroll
-        for (int c = 0; c < kCols; c += 32)
-          tc::tmem_load32(tmem + (uint32_t(32 * q) << 16) + acc * kN + h * kCols + c, v + c);
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        const int64_t c0 = int64_t(n) * kN + h * kCols;
-        if (c0 + kCols > p.V) {  // the tile that crosses V: W's rows past V load as zeros
+        for (int hh = 0; hh < kCols / 32; ++hh) {
+          float v[32];
+          tc::tmem_load32(tmem + (uint32_t(32 * q) << 16) + acc * kN + h * kCols + 32 * hh, v);
+          if (hh == kCols / 32 - 1) {  // the accumulator is free once every column is loaded
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          }
+          const int64_t c0 = int64_t(n) * kN + h * kCols + 32 * hh;
+          if (c0 + 32 > p.V) {  // the tile that crosses V: W's rows past V load as zeros
 #pragma unroll
-          for (int c = 0; c < kCols; ++c)
-            if (c0 + c >= p.V) v[c] = -INFINITY;
+            for (int c = 0; c < 32; ++c)
+              if (c0 + c >= p.V) v[c] = -INFINITY;
+          }
+          const int64_t dx = int64_t(x) - c0;
+          if (dx >= 0 && dx < 32) {
+            float val = v[0];
+#pragma unroll
+            for (int c = 1; c < 32; ++c)
+              if (c == dx) val = v[c];
+            xl = val;
+            xf = 1.f;
+          }
+          // log2-domain statistics: one rescale per 32 columns, then 2^(v log2e - m2) each
+          float tmax = v[0];
+#pragma unroll
+          for (int c = 1; c < 32; ++c) tmax = fmaxf(tmax, v[c]);
+          const float vm = tmax * kLog2e;
+          if (vm > m2) {
+            sum *= fast_exp2(m2 - vm);
+            m2 = vm;
+          }
+          const float2 l2 = splat2(kLog2e), nm = splat2(-m2);
+          float2 tot = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float2 e0 = exp2_2(fma2(make_float2(v[c], v[c + 1]), l2, nm));
+            const float2 e1 = exp2_2(fma2(make_float2(v[c + 2], v[c + 3]), l2, nm));
+            tot = add2(tot, add2(e0, e1));
+          }
+          sum += tot.x + tot.y;
+          // race candidates: the target slot takes columns 0..15 of the 32, the draft slot
+          // 16..31, each with both logits of its entries.  In place: afterwards v[0..15] holds the
+          // target logits and v[16..31] the draft logits of this lane's 16 entries.
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float recv = __shfl_xor_sync(0xffffffffu, kind ? v[c] : v[16 + c], 1);
+            if (kind)
+              v[c] = recv;
+            else
+              v[16 + c] = recv;
+          }
+          if (mode) cand_offer16(cl, st, v, v + 16, c0 + (kind ? 16 : 0), G);
         }
-        const int64_t dx = int64_t(x) - c0;
-        if (dx >= 0 && dx < kCols) {
-          float val = v[0];
-#pragma unroll
-          for (int c = 1; c < kCols; ++c)
-            if (c == dx) val = v[c];
-          xl = val;
-          xf = 1.f;
+        if (mode) {
+          const float last = cl.amin;  // -inf until the list is full
+          if (last > published && last > G) {
+            atomicMax(cslot, key_order(last));
+            published = last;
+          }
+          G = key_from_order(__ldcg(cslot));  // used from the next tile on
         }
-        // log2-domain statistics: one rescale per tile, then 2^(v log2e - m2) per column
-        float tmax = v[0];
-#pragma unroll
-        for (int c = 1; c < kCols; ++c) tmax = fmaxf(tmax, v[c]);
-        const float vm = tmax * kLog2e;
-        if (vm > m2) {
-          sum *= fast_exp2(m2 - vm);
-          m2 = vm;
-        }
-        const float2 l2 = splat2(kLog2e), nm = splat2(-m2);
-        float2 tot = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < kCols; c += 4) {
-          const float2 e0 = exp2_2(fma2(make_float2(v[c], v[c + 1]), l2, nm));
-          const float2 e1 = exp2_2(fma2(make_float2(v[c + 2], v[c + 3]), l2, nm));
-          tot = add2(tot, add2(e0, e1));
-        }
-        sum += tot.x + tot.y;
       }
+      if (mode) {
+        const size_t pp = (size_t(r) * (p.gmax + 1) + j) * p.per_mblock + ci;
+        const int part = h * 2 + kind;
+        float4* dst = p.cand + (pp * kLmParts + part) * kLmCand;
+#pragma unroll
+        for (int i = 0; i < kLmCand; ++i) {
+          const float2 bx = cl.bx[i * kBxStride];
+          dst[i] = make_float4(cl.a[i], bx.x, bx.y, 0.f);
+        }
+        // every entry this lane did not keep has a plain key no larger than its last kept one or
+        // than the gate key it was dropped against
+        p.theta[pp * kLmParts + part] = fmaxf(cl.amin, gate_max);
+      }
+      named_sync(1, 32 * kLmEpiWarps);  // the candidate buffer becomes the merge area
       if (h > 0) merge[h - 1][rl] = make_float4(m2, sum, xl, xf);
       named_sync(1, 32 * kLmEpiWarps);
       if (h == 0) {
@@ -338,6 +537,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       // race: the target slot keys the first half of each warp's columns, the draft slot the
       // second half, each with both logits of its entries (one exchange per column)
       constexpr int kHalf = kCols / 2;
+      const int32_t qi = R >> 1;  // queue slot
+      const bool row_ok = qi < queued;
+      const int32_t r = row_ok ? p.race_list[qi] : 0;
       RaceDesc d = {0, 0, 0.f, 0};
       if (row_ok) d = p.desc[r];
       RaceSpec rs;
@@ -484,6 +686,13 @@ struct LmWs {
   RaceDesc* desc;         // [B]
   uint32_t* k0;           // [B]
   unsigned long long* winners;  // [per2][B][2]
+  float4* cand;           // [B (gmax + 1)][per1][kLmParts][kLmCand]
+  float* theta;           // [B (gmax + 1)][per1][kLmParts]
+  unsigned long long* decided;  // [B]
+  int32_t* pending;       // [B]
+  int32_t* race_list;     // [B]
+  int32_t* race_count;    // [1]
+  uint32_t* cpub;         // [B (gmax + 1)]
   size_t total;
 };
 
@@ -505,6 +714,14 @@ LmWs lm_layout(void* base, int32_t B, int32_t gmax, int64_t H, const LmGeom& g) 
   w.k0 = reinterpret_cast<uint32_t*>(take(sizeof(uint32_t) * size_t(B)));
   w.winners = reinterpret_cast<unsigned long long*>(
       take(sizeof(unsigned long long) * 2 * size_t(B) * size_t(g.per2)));
+  const size_t parts = size_t(B) * size_t(gmax + 1) * size_t(g.per1) * kLmParts;
+  w.cand = reinterpret_cast<float4*>(take(sizeof(float4) * parts * kLmCand));
+  w.theta = reinterpret_cast<float*>(take(sizeof(float) * parts));
+  w.decided = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * size_t(B)));
+  w.pending = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * size_t(B)));
+  w.race_list = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * size_t(B)));
+  w.race_count = reinterpret_cast<int32_t*>(take(sizeof(int32_t)));
+  w.cpub = reinterpret_cast<uint32_t*>(take(sizeof(uint32_t) * size_t(B) * size_t(gmax + 1)));
   w.total = off;
   return w;
 }
@@ -540,8 +757,8 @@ extern "C" sv_status spec_verify_lmhead(
     int64_t H, int64_t V, const int64_t* target_row0, const int64_t* draft_row0,
     const int32_t* draft_len, int32_t max_draft_len, const int32_t* draft_tokens, int32_t B,
     uint64_t seed, const uint64_t* request_ids, int32_t* accepted_len, int32_t* out_tokens,
-    int64_t out_ld, int32_t* correction_token, float* accept_ratio, int32_t* status,
-    void* workspace, size_t workspace_bytes, void* stream) {
+    int64_t out_ld, int32_t* correction_token, float* accept_ratio, int32_t* recomputed,
+    int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
   if (B < 0 || max_draft_len < 0 || max_draft_len > SV_MAX_DRAFT_LEN || V < 1 || H < 1)
     return SV_ERR_INVALID;
   if (H % 64 != 0 || V > (int64_t(1) << 31) - kLmStatsN) return SV_ERR_UNSUPPORTED;
@@ -588,7 +805,7 @@ extern "C" sv_status spec_verify_lmhead(
   profile_mark(0, s);
   lm_gather_kernel<<<B, 256, 0, s>>>(
       static_cast<const uint8_t*>(target_hidden), static_cast<const uint8_t*>(draft_hidden), ldh,
-      H, target_row0, draft_row0, draft_len, gmax, ws.A1, status);
+      H, target_row0, draft_row0, draft_len, gmax, ws.A1, ws.cpub, ws.race_count, status);
   sv_status st = launch_status(cudaGetLastError());
   if (st != SV_OK) return st;
 
@@ -607,6 +824,11 @@ extern "C" sv_status spec_verify_lmhead(
   p.request_ids = request_ids;
   p.k0 = ws.k0;
   p.winners = ws.winners;
+  p.cand = ws.cand;
+  p.theta = ws.theta;
+  p.cpub = ws.cpub;
+  p.race_count = ws.race_count;
+  p.race_list = ws.race_list;
   p.status = status;
   {
     LmParams p1 = p;
@@ -641,6 +863,13 @@ extern "C" sv_status spec_verify_lmhead(
   dq.desc = ws.desc;
   dq.k0 = ws.k0;
   dq.accepted_len = accepted_len;
+  dq.cand = ws.cand;
+  dq.theta = ws.theta;
+  dq.C = g.per1;
+  dq.decided = ws.decided;
+  dq.pending = ws.pending;
+  dq.race_count = ws.race_count;
+  dq.race_list = ws.race_list;
   lm_decide_kernel<<<B, kThreads, 0, s>>>(dq);
   st = launch_status(cudaGetLastError());
   if (st != SV_OK) return st;
@@ -657,7 +886,12 @@ extern "C" sv_status spec_verify_lmhead(
   }
   winners_finish_kernel<<<unsigned((B + 127) / 128), 128, 0, s>>>(
       ws.winners, g.per2, B, accepted_len, draft_row0, draft_tokens, out_tokens, out_ld,
-      correction_token, status);
+      correction_token, status, ws.pending, ws.decided);
+  st = launch_status(cudaGetLastError());
+  if (st != SV_OK) return st;
+  if (recomputed && cudaMemcpyAsync(recomputed, ws.race_count, sizeof(int32_t),
+                                    cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return SV_ERR_CUDA;
   profile_mark(3, s);
   return launch_status(cudaGetLastError());
 }

@@ -659,19 +659,26 @@ static sv_status launch_race(RaceParams rp, cudaStream_t stream) {
 // The largest of n partial race winners per request -- the largest of the race over p if no
 // partial had a residual entry -- and the request's outputs.  winners_all is [n][B][2] packed
 // results (race_pack; 0: none), the residual (or bonus) winner first, the race over p second.
-// One thread per request.
+// With `pending` set, a request whose pending[r] is 0 was decided before: its packed winner is
+// decided[r] and winners_all is not read for it.  One thread per request.
 template <int kDummy = 0>
 __global__ void winners_finish_kernel(const unsigned long long* winners_all, int32_t n,
                                       int32_t B, const int32_t* accepted_len,
                                       const int64_t* draft_row0, const int32_t* draft_tokens,
                                       int32_t* out_tokens, int64_t out_ld,
-                                      int32_t* correction_token, int32_t* status) {
+                                      int32_t* correction_token, int32_t* status,
+                                      const int32_t* pending = nullptr,
+                                      const unsigned long long* decided = nullptr) {
   const int32_t r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= B) return;
   unsigned long long best = 0ull, fb = 0ull;
-  for (int32_t k = 0; k < n; ++k) {
-    best = max(best, winners_all[(size_t(k) * B + r) * 2]);
-    fb = max(fb, winners_all[(size_t(k) * B + r) * 2 + 1]);
+  if (pending && !pending[r]) {
+    best = decided[r];
+  } else {
+    for (int32_t k = 0; k < n; ++k) {
+      best = max(best, winners_all[(size_t(k) * B + r) * 2]);
+      fb = max(fb, winners_all[(size_t(k) * B + r) * 2 + 1]);
+    }
   }
   if (!best) best = fb;
   const int32_t y = best ? race_unpack_index(best) : -1;

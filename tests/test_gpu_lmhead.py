@@ -69,6 +69,7 @@ def _parity(sv, orc, inp, request_ids=None):
     gpu = _gpu(sv, inp, tokens, request_ids)
     res = compare_verify(gpu, ref, False, inp["draft_len"].numpy(), inp["draft_row0"].numpy(),
                          near_tie=LOGIT_TIE, rel_tol=RATIO_TOL)
+    res["recomputed"] = int(gpu["recomputed"].item())
     print(f"\n[lmhead parity] B={inp['B']} V={inp['V']} H={inp['H']}: {res}")
     return gpu, ref, res
 
@@ -102,6 +103,50 @@ def test_lmhead_no_drafts(sv, orc):
     inp = synth.lmhead_inputs(w)
     gpu, ref, _ = _parity(sv, orc, inp)
     assert (gpu["accepted_len"].cpu().numpy() == 0).all()
+
+
+def _adversarial_inputs(B, gamma, V, H, seed, gen_seed):
+    """Hidden rows whose residual mass hides behind the largest plain keys.  Logits are N(0, 1)
+    except the 32 tokens {0..15, 32..47}: target logit 7 (+ N(0, 0.3^2)), draft logit 4 higher.
+    The draft puts almost all of q on those tokens, so a drafted token is rejected with
+    probability about 0.08 per position, and the correction then comes from the other tokens,
+    whose plain keys sit far below the top tokens' -- the case the first pass's candidates often
+    cannot settle, so the correction is recomputed.  Column 0 carries the constant logit offsets,
+    column 1 the draft's extra offset, the rest the N(0, 1) part."""
+    g = torch.Generator().manual_seed(gen_seed)
+    top = torch.zeros(V, dtype=torch.bool)
+    top[0:16] = True
+    top[32:48] = True
+    W = torch.randn((V, H), generator=g) / np.sqrt(H - 2)
+    W[:, 0] = 0.0
+    W[:, 1] = 0.0
+    W[top, 0] = 7.0
+    W[top, 1] = 4.0
+    W[top, 2:] *= 0.3
+    target = torch.randn((B * (gamma + 1), H), generator=g)
+    target[:, 0] = 1.0
+    target[:, 1] = 0.0
+    draft = target.view(B, gamma + 1, H)[:, :gamma, :].reshape(B * gamma, H).clone()
+    draft[:, 1] = 1.0
+    return {
+        "target_hidden": target.to(torch.bfloat16), "draft_hidden": draft.to(torch.bfloat16),
+        "W": W.to(torch.bfloat16), "V": V, "H": H,
+        "target_row0": torch.arange(B, dtype=torch.int64) * (gamma + 1),
+        "draft_row0": torch.arange(B, dtype=torch.int64) * gamma,
+        "draft_len": torch.full((B,), gamma, dtype=torch.int32),
+        "max_draft_len": gamma, "B": B, "seed": seed,
+    }
+
+
+def test_lmhead_recomputed_corrections(sv, orc):
+    """Corrections the candidates cannot settle go through the second pass, and agree with the
+    oracle like the rest."""
+    inp = _adversarial_inputs(48, 6, 2053, 192, 21, 1011)
+    gpu, ref, res = _parity(sv, orc, inp)
+    n = int(gpu["recomputed"].item())
+    print(f"[lmhead] recomputed corrections: {n} of {inp['B']}")
+    assert n > 0
+    assert n <= int((ref["accepted_len"] < inp["max_draft_len"]).sum())
 
 
 def test_lmhead_full_size_sampled(sv, orc):

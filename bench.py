@@ -46,7 +46,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the supplementary rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["markov", "schedule", "block"], default=None,
+    ap.add_argument("--only", choices=["markov", "schedule", "block", "lmhead"], default=None,
                     help="time one supplementary row alone and print it (profiling runs)")
     ap.add_argument("--markov-positions", type=int, default=None,
                     help="with --only markov: draft this many positions instead of 16")
@@ -452,6 +452,7 @@ def bench_rows(steps, warmup):
     del vin, vt
 
     rows["markov_draft_256x16_V151936_R256"] = bench_markov(steps, warmup, flush, stream)
+    rows["lmhead_verify_64x5_V151936_H2560_bf16"] = bench_lmhead(steps, warmup, flush, stream)
     return rows
 
 
@@ -607,6 +608,72 @@ def bench_markov(steps, warmup, flush, stream, positions=None):
         "launches_per_call": 2 * w.K, "status": int(status.item())}
 
 
+def bench_lmhead(steps, warmup, flush, stream):
+    """Verification from hidden states: 64 requests x 5 drafted positions, V = 151936, H = 2560,
+    bf16 hidden rows and output projection (spec_verify_lmhead).  Algorithmic work per call: the
+    logits of the B (2 gamma + 1) target and draft rows, 2 Q H V FLOPs ("How much does a token
+    cost", "The Role of Arithmetic Intensity"), and one read of W plus the hidden rows."""
+    import torch
+    import speculative_decoding_verification_token_gb300 as sv
+    from speculative_decoding_verification_token_gb300 import synth
+    w = synth.LMHEAD
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = synth.lmhead_inputs(w, device=dev)
+    # drafted tokens (setup, untimed): the draft's logits through W, sampled by the library
+    dlog = inp["draft_hidden"].float() @ inp["W"].float().t()
+    tokens = sv.spec_sample_draft(dlog, inp["draft_row0"], inp["draft_len"], w.gamma, w.seed)
+    del dlog
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = sv.workspace(sv.spec_verify_lmhead_workspace_bytes(w.B, w.gamma, w.V, w.H), dev)
+    holder = {}
+
+    def call():
+        holder["o"] = sv.spec_verify_lmhead(inp["target_hidden"], inp["draft_hidden"], inp["W"],
+                                            inp["target_row0"], inp["draft_row0"],
+                                            inp["draft_len"], w.gamma, tokens, w.seed,
+                                            status=status, workspace=ws)
+    t = time_calls(call, steps, warmup, flush, stream)
+    st = int(status.item())
+    out = holder["o"]
+    sv.sv_profile_enable(True)
+    parts = []
+    for _ in range(max(3, steps // 2)):
+        flush()
+        call()
+        parts.append(sv.sv_profile_read())
+    sv.sv_profile_enable(False)
+    kms = [sum(q[k] for q in parts) / len(parts) for k in range(3)]
+    # context only, not part of the path: the same logits as one cuBLAS bf16 GEMM (bf16 output),
+    # the first step of a pipeline that stores logits and verifies them afterwards
+    rows = w.B * (2 * w.gamma + 1)
+    hidden = torch.randn((rows, w.H), device=dev, dtype=torch.bfloat16)
+    Wt = inp["W"].t()
+    t_gemm = time_calls(lambda: hidden @ Wt, steps, warmup, flush, stream)
+    del hidden
+    tm = sum(t) / len(t)
+    flops = 2.0 * rows * w.H * w.V
+    slots = -(-w.B * 2 * (w.gamma + 1) // 128) * 128
+    w_bytes = w.V * w.H * 2
+    peaks, _ = measured_peaks()
+    tf = float(peaks["bf16_tflops"])
+    return {
+        "workload": f"{w.B} requests x {w.gamma} positions, V={w.V}, H={w.H}, bf16",
+        "ms": tm * 1e3, "ms_median": statistics.median(t) * 1e3,
+        "positions_per_s": w.B * w.gamma / tm,
+        "algorithmic_flops_per_call": flops,
+        "TFLOP_s": flops / tm / 1e12, "tensor_frac_of_measured": flops / tm / 1e12 / tf,
+        "computed_flops_per_call": 2.0 * slots * w.H * w.V,
+        "W_bytes_per_call": w_bytes, "W_GB_s": w_bytes / tm / 1e9,
+        "kernel_ms": {"gather_and_statistics_gemm": round(kms[0], 4),
+                      "decide": round(kms[1], 4), "race_gemm_and_finish": round(kms[2], 4)},
+        "kernel_ms_note": "from a separate run with CUDA events between the library's kernels "
+                          "(serialised, no programmatic overlap)",
+        "recomputed_requests": int(out["recomputed"].item()),
+        "mean_accepted": float(out["accepted_len"].float().mean()),
+        "context_cublas_logits_gemm_bf16_out_ms": sum(t_gemm) / len(t_gemm) * 1e3,
+        "status": st}
+
+
 # ---- main ----------------------------------------------------------------------------------------
 
 def main():
@@ -644,6 +711,11 @@ def main():
     if args.only == "schedule":
         row = bench_schedule(args.steps, args.warmup)
         print(json.dumps({"row": "schedule", **row}))
+        return
+    if args.only == "lmhead":
+        row = bench_lmhead(args.steps, args.warmup, make_flush(torch.device("cuda")),
+                           torch.cuda.current_stream())
+        print(json.dumps({"row": "lmhead_verify", **row}))
         return
 
     res = bench_token(args, rank, world, peaks, peak_src)

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(256)
                      const int64_t* __restrict__ draft_row0, const int32_t* __restrict__ draft_len,
                      int32_t gmax, uint8_t* __restrict__ A, uint32_t* cpub,
                      int32_t* race_count, int32_t* status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int32_t r = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (r == 0 && threadIdx.x == 0) {
@@ -241,6 +242,8 @@ __global__ void __launch_bounds__(kThreads) lm_decide_kernel(LmDecideParams p) {
   __shared__ float red_k[kWarps];
   __shared__ int32_t red_i[kWarps];
   __shared__ int32_t s_slot;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the statistics GEMM's partials
   const int32_t r = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   decide_body<float>(p.dp, r, true, &s_desc, s_tok, false);
@@ -312,8 +315,12 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   const int32_t ci = blockIdx.x / p.n_mblocks;
   const int32_t m0 = mb * kLmRows;
   const int32_t n_my = ci < p.n_tiles ? (p.n_tiles - ci + p.per_mblock - 1) / p.per_mblock : 0;
+  // programmatic dependent of the kernel before it (gather, resp. decide): its outputs are read
+  // only after griddepcontrol.wait, which every CTA executes before it exits
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int32_t queued = 0;  // race GEMM: requests in the queue (two slots each)
   if constexpr (kRace) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     queued = *reinterpret_cast<const volatile int32_t*>(p.race_count);
     if (m0 >= 2 * queued) return;  // the whole CTA: nothing allocated or initialised yet
   }
@@ -330,6 +337,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) tc::tmem_alloc(&tmem_base, Sh::kTmemCols);
+  if constexpr (!kRace) asm volatile("griddepcontrol.wait;" ::: "memory");  // the slot block
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -726,6 +734,24 @@ LmWs lm_layout(void* base, int32_t B, int32_t gmax, int64_t H, const LmGeom& g) 
   return w;
 }
 
+// A programmatic dependent launch: the kernel may start while the one before it finishes, and
+// waits for it (griddepcontrol.wait) before touching its outputs.
+template <typename... KArgs, typename... Args>
+sv_status launch_pdl(void (*kernel)(KArgs...), int grid, int threads, size_t smem, cudaStream_t s,
+                     Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return launch_status(cudaLaunchKernelEx(&cfg, kernel, args...));
+}
+
 template <int kN, bool kRace>
 sv_status launch_lm_gemm(const CUtensorMap& map_a, const CUtensorMap& map_w, const LmParams& p,
                          cudaStream_t s) {
@@ -734,8 +760,7 @@ sv_status launch_lm_gemm(const CUtensorMap& map_a, const CUtensorMap& map_w, con
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(Sh::kSmem)) != cudaSuccess)
     return SV_ERR_CUDA;
-  kern<<<p.n_mblocks * p.per_mblock, kLmThreads, Sh::kSmem, s>>>(map_a, map_w, p);
-  return launch_status(cudaGetLastError());
+  return launch_pdl(kern, p.n_mblocks * p.per_mblock, kLmThreads, Sh::kSmem, s, map_a, map_w, p);
 }
 
 }  // namespace
@@ -870,8 +895,7 @@ extern "C" sv_status spec_verify_lmhead(
   dq.pending = ws.pending;
   dq.race_count = ws.race_count;
   dq.race_list = ws.race_list;
-  lm_decide_kernel<<<B, kThreads, 0, s>>>(dq);
-  st = launch_status(cudaGetLastError());
+  st = launch_pdl(lm_decide_kernel, B, kThreads, 0, s, dq);
   if (st != SV_OK) return st;
   profile_mark(2, s);
 
@@ -884,10 +908,11 @@ extern "C" sv_status spec_verify_lmhead(
     st = launch_lm_gemm<kLmRaceN, true>(map_a2, map_w2, p2, s);
     if (st != SV_OK) return st;
   }
-  winners_finish_kernel<<<unsigned((B + 127) / 128), 128, 0, s>>>(
-      ws.winners, g.per2, B, accepted_len, draft_row0, draft_tokens, out_tokens, out_ld,
-      correction_token, status, ws.pending, ws.decided);
-  st = launch_status(cudaGetLastError());
+  st = launch_pdl(winners_finish_kernel<0>, (B + 127) / 128, 128, 0, s,
+                  static_cast<const unsigned long long*>(ws.winners), g.per2, B,
+                  static_cast<const int32_t*>(accepted_len), draft_row0, draft_tokens, out_tokens,
+                  out_ld, correction_token, status, static_cast<const int32_t*>(ws.pending),
+                  static_cast<const unsigned long long*>(ws.decided));
   if (st != SV_OK) return st;
   if (recomputed && cudaMemcpyAsync(recomputed, ws.race_count, sizeof(int32_t),
                                     cudaMemcpyDeviceToDevice, s) != cudaSuccess)

@@ -669,6 +669,8 @@ __global__ void winners_finish_kernel(const unsigned long long* winners_all, int
                                       int32_t* correction_token, int32_t* status,
                                       const int32_t* pending = nullptr,
                                       const unsigned long long* decided = nullptr) {
+  // launched as a programmatic dependent or not: the wait is a no-op in the second case
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int32_t r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= B) return;
   unsigned long long best = 0ull, fb = 0ull;

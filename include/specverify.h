@@ -2,8 +2,9 @@
  * specverify.h -- C ABI of the GB300 speculative-decoding verification library.
  *
  * The library turns target and draft logits into verified tokens (token-level and block
- * verification), drafts a block with DSpark's Markov head, and schedules how much of each drafted
- * block to verify.  Every call is one or more hand-written CUDA kernels for sm_103a launched on the
+ * verification, also with the vocabulary split across ranks, or straight from hidden states
+ * through an output projection), drafts a block with DSpark's Markov head, and schedules how much
+ * of each drafted block to verify.  Every call is one or more hand-written CUDA kernels for sm_103a launched on the
  * caller's stream.
  *
  * Conventions for every entry point

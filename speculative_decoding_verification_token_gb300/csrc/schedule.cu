@@ -1,22 +1,25 @@
-// schedule.cu -- DSpark's hardware-aware prefix scheduler: two kernels on the caller's stream.
+// schedule.cu -- DSpark's hardware-aware prefix scheduler: three kernels on the caller's stream.
 //
-//   rank   (every SM; one warp per extendable prefix)  each CTA stages the conditional acceptance
-//          probabilities in shared memory (coalesced), forms the survival products
-//          S[i][k] = c[i][1] * ... * c[i][k] (sequential binary32, one thread per request) and one
-//          64-bit key per extendable prefix (i, k):
+//   chunk  (one CTA per 32 requests)  one thread per request forms the survival products
+//          S[i][k] = c[i][1] * ... * c[i][k] (sequential binary32) and one 64-bit key per
+//          extendable prefix (i, k):
 //            key = (~bits(S) << 32) | (k << 20) | i
 //          ascending keys order prefixes by S descending, then k ascending, then i ascending (S >= 0,
 //          whose bit patterns are monotone in the value).  S never grows with k, so each request's
-//          keys form an ascending run, and the rank of a prefix in the global order is the sum over
-//          the runs of the number of their keys below its own -- one binary search per run, the
-//          lanes of a warp splitting the runs.  The rank places F = floor(S * 2^40) in sorted order
-//          and is kept per prefix.
+//          keys form an ascending run; the CTA merges its runs pairwise in shared memory into one
+//          sorted chunk.
+//   rank   (every SM, a programmatic dependent of chunk)  each CTA stages the sorted chunks; the
+//          rank of a key in the global order is its place in its own chunk plus one binary search
+//          in every other chunk.  The rank places F = floor(S * 2^40) and the request in sorted
+//          order.
 //   admit  (one CTA, a programmatic dependent of rank)  an exclusive int64 scan of F in sorted
 //          order gives T(b) = N * 2^40 + (sum of the first b values of F), exact and independent of
 //          the summation order; f(b) = (double) T(b) * 2^-40 * sps[N + b]; the admitted count b* is
-//          the first b with f(b + 1) <= f(b) (early stop; a min-reduction over b), capped by the
-//          item count and by B_max; sel_len[i] counts the prefixes of request i ranked below b*
-//          (prefix-closed by the ordering).
+//          the first b with f(b + 1) <= f(b) (early stop; a min-reduction over b), or the smallest b
+//          of largest f(b) (best budget), capped by the item count and by B_max; sel_len[i] counts
+//          the prefixes of request i ranked below b* (prefix-closed by the ordering).
+// The fixed-depth rule needs no ranking (depth kernel), and the per-position acceptance update is a
+// kernel of its own.
 #include <algorithm>
 #include <cstdint>
 

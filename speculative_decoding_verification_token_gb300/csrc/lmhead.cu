@@ -88,40 +88,55 @@ struct LmParams {
   int32_t* status;
 };
 
-// Copies of hidden rows: one warp per row, 16-byte vectors.
+// Copies of hidden rows: one warp per row, 16-byte vectors, four loads in flight per lane.
 __device__ __forceinline__ void copy_row(uint8_t* dst, const uint8_t* src, int64_t bytes,
                                          int lane) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
   uint4* d = reinterpret_cast<uint4*>(dst);
-  for (int64_t i = lane; i < bytes / 16; i += 32) d[i] = __ldg(s + i);
+  const int64_t n = bytes / 16;
+  int64_t i = lane;
+  for (; i + 96 < n; i += 128) {
+    const uint4 a0 = __ldg(s + i), a1 = __ldg(s + i + 32), a2 = __ldg(s + i + 64),
+                a3 = __ldg(s + i + 96);
+    d[i] = a0;
+    d[i + 32] = a1;
+    d[i + 64] = a2;
+    d[i + 96] = a3;
+  }
+  for (; i < n; i += 32) d[i] = __ldg(s + i);
 }
 
+constexpr int kGatherWarps = 8;
+
 // Slot block of the statistics GEMM: request r's target row j into slot r S + 2j (j <= g), its
-// draft row j into slot r S + 2j + 1 (j < g).  One CTA per request, which also clears the
-// request's published candidate bounds; block 0 clears the status and the race queue.
-__global__ void __launch_bounds__(256)
+// draft row j into slot r S + 2j + 1 (j < g); one warp per (request, slot).  The first warp of
+// each request also clears its published candidate bounds; block 0 clears the status and the race
+// queue.
+__global__ void __launch_bounds__(32 * kGatherWarps)
     lm_gather_kernel(const uint8_t* __restrict__ th, const uint8_t* __restrict__ dh, int64_t ldh,
                      int64_t H, const int64_t* __restrict__ target_row0,
                      const int64_t* __restrict__ draft_row0, const int32_t* __restrict__ draft_len,
-                     int32_t gmax, uint8_t* __restrict__ A, uint32_t* cpub,
+                     int32_t B, int32_t gmax, uint8_t* __restrict__ A, uint32_t* cpub,
                      int32_t* race_count, int32_t* status) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int32_t r = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (r == 0 && threadIdx.x == 0) {
+  const int lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
     *race_count = 0;
     if (status) *status = 0;
   }
-  for (int32_t j = threadIdx.x; j <= gmax; j += blockDim.x) cpub[size_t(r) * (gmax + 1) + j] = 0u;
+  const int32_t per = 2 * gmax + 1;  // rows a request may have
+  const int64_t w = int64_t(blockIdx.x) * kGatherWarps + (threadIdx.x >> 5);
+  if (w >= int64_t(B) * per) return;
+  const int32_t r = static_cast<int32_t>(w / per);
+  const int32_t s = static_cast<int32_t>(w % per);
+  if (s == 0)
+    for (int32_t j = lane; j <= gmax; j += 32) cpub[size_t(r) * (gmax + 1) + j] = 0u;
   const int32_t g = clamp_gamma(draft_len[r], gmax);
-  const int32_t S = 2 * (gmax + 1);
-  const int64_t row_bytes = H * 2;
-  for (int32_t s = warp; s < 2 * g + 1; s += 8) {
-    const int32_t j = s >> 1;
-    const uint8_t* src = (s & 1) ? dh + (draft_row0[r] + j) * ldh * 2
-                                 : th + (target_row0[r] + j) * ldh * 2;
-    copy_row(A + (int64_t(r) * S + s) * row_bytes, src, row_bytes, lane);
-  }
+  if (s >= 2 * g + 1) return;
+  const int32_t j = s >> 1;
+  const uint8_t* src = (s & 1) ? dh + (draft_row0[r] + j) * ldh * 2
+                               : th + (target_row0[r] + j) * ldh * 2;
+  copy_row(A + (int64_t(r) * 2 * (gmax + 1) + s) * H * 2, src, H * 2, lane);
 }
 
 struct KeyIdx {
@@ -253,17 +268,27 @@ __global__ void __launch_bounds__(kThreads) lm_decide_kernel(LmDecideParams p) {
   const int32_t n_parts = p.C * kLmParts;
   const float4* cd = p.cand + u2 * n_parts * kLmCand;
   KeyIdx best = {-INFINITY, -1};
-  for (int32_t i = tid; i < n_parts * kLmCand; i += kThreads) {
-    const float4 q = cd[i];
+  auto offer_cand = [&](const float4& q) {
     const int32_t e = __float_as_int(q.z);
-    if (e < 0) continue;
+    if (e < 0) return;
     if (!d.resid) {
       offer_key(q.x, e, best);
     } else {
       const float y = q.y + d.gap;
       if (y < 0.f) offer_key(q.x + __logf(one_minus_exp(y)), e, best);
     }
+  };
+  const int32_t n_cand = n_parts * kLmCand;
+  int32_t i = tid;
+  for (; i + 3 * kThreads < n_cand; i += 4 * kThreads) {  // four loads in flight
+    const float4 q0 = cd[i], q1 = cd[i + kThreads], q2 = cd[i + 2 * kThreads],
+                 q3 = cd[i + 3 * kThreads];
+    offer_cand(q0);
+    offer_cand(q1);
+    offer_cand(q2);
+    offer_cand(q3);
   }
+  for (; i < n_cand; i += kThreads) offer_cand(cd[i]);
   float bound = -INFINITY;  // largest plain key an unkept entry may have
   for (int32_t i = tid; i < n_parts; i += kThreads) bound = fmaxf(bound, p.theta[u2 * n_parts + i]);
   block_race<kThreads>(best.key, best.idx, red_k, red_i);
@@ -828,9 +853,11 @@ extern "C" sv_status spec_verify_lmhead(
   }
 
   profile_mark(0, s);
-  lm_gather_kernel<<<B, 256, 0, s>>>(
+  const int64_t gather_warps = int64_t(B) * (2 * gmax + 1);
+  lm_gather_kernel<<<unsigned((gather_warps + kGatherWarps - 1) / kGatherWarps),
+                     32 * kGatherWarps, 0, s>>>(
       static_cast<const uint8_t*>(target_hidden), static_cast<const uint8_t*>(draft_hidden), ldh,
-      H, target_row0, draft_row0, draft_len, gmax, ws.A1, ws.cpub, ws.race_count, status);
+      H, target_row0, draft_row0, draft_len, B, gmax, ws.A1, ws.cpub, ws.race_count, status);
   sv_status st = launch_status(cudaGetLastError());
   if (st != SV_OK) return st;
 

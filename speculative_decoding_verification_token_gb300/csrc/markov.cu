@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   const int32_t ci = blockIdx.x / p.n_mblocks;
   const int32_t m0 = mb * kMkRows;
   const int32_t n_my = ci < p.n_tiles ? (p.n_tiles - ci + p.per_mblock - 1) / p.per_mblock : 0;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (tid == 0) {
     s_bad = 0;
@@ -174,6 +175,9 @@ __global__ void __launch_bounds__(kMkThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) tc::tmem_alloc(&tmem_base, kMkTmemCols);
+  // A programmatic dependent of the previous position's select kernel: x_{k-1} and the partials
+  // it reads are touched only after it has finished.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // A operand: the 128 rows U[x_{k-1}] in the swizzled K-major layout (rows past B use row 0)
   {
@@ -434,6 +438,9 @@ __global__ void __launch_bounds__(256)
                          int32_t K, int32_t k, const float* __restrict__ conf_scores,
                          const float* __restrict__ sts_T, int32_t* tokens, float* row_stats,
                          float* conf_out, int32_t* status) {
+  // a programmatic dependent of the position kernel: its partials are read after it has finished
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int32_t b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= B) return;
@@ -576,14 +583,36 @@ extern "C" sv_status dspark_markov_draft(const void* backbone_logits, int64_t ld
   if (cudaMemsetAsync(bounds, 0, size_t(K) * B * sizeof(uint32_t), cs) != cudaSuccess)
     return SV_ERR_CUDA;
   profile_mark(0, cs);
+  // every launch after the first is a programmatic dependent of the one before (it starts while
+  // that one finishes and waits for it with griddepcontrol.wait before touching its outputs)
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t pos_cfg = {};
+  pos_cfg.gridDim = dim3(grid);
+  pos_cfg.blockDim = dim3(kMkThreads);
+  pos_cfg.dynamicSmemBytes = kMkSmem;
+  pos_cfg.stream = cs;
+  cudaLaunchConfig_t sel_cfg = pos_cfg;
+  sel_cfg.gridDim = dim3(sel_grid);
+  sel_cfg.blockDim = dim3(256);
+  sel_cfg.dynamicSmemBytes = 0;
+  sel_cfg.attrs = pdl;
+  sel_cfg.numAttrs = 1;
   for (int32_t k = 1; k <= K; ++k) {
     p.k = k;
     p.k0 = bounds + size_t(k - 1) * B;
-    markov_position_kernel<0><<<grid, kMkThreads, kMkSmem, cs>>>(map_wt, map_bb, map_z, p);
+    pos_cfg.attrs = k > 1 ? pdl : nullptr;
+    pos_cfg.numAttrs = k > 1 ? 1 : 0;
+    if (cudaLaunchKernelEx(&pos_cfg, markov_position_kernel<0>, map_wt, map_bb, map_z, p) !=
+        cudaSuccess)
+      return SV_ERR_CUDA;
     if (k == 1) profile_mark(1, cs);
-    markov_select_kernel<<<sel_grid, 256, 0, cs>>>(p.partials, g.per_mblock, B, K, k, conf_scores,
-                                                   sts_T, draft_tokens, row_stats, conf_out,
-                                                   status);
+    if (cudaLaunchKernelEx(&sel_cfg, markov_select_kernel,
+                           static_cast<const MkPartial*>(p.partials), g.per_mblock, B, K, k,
+                           conf_scores, sts_T, draft_tokens, row_stats, conf_out, status) !=
+        cudaSuccess)
+      return SV_ERR_CUDA;
     if (k == 1) profile_mark(2, cs);
   }
   profile_mark(3, cs);

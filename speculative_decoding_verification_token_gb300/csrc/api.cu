@@ -1,4 +1,6 @@
 // api.cu -- status strings, version and the host-side device queries used by every entry point.
+#include <atomic>
+#include <chrono>
 #include <mutex>
 
 #include "sv_device.cuh"
@@ -37,6 +39,14 @@ int device_smem_per_sm() {
     g_smem_per_sm[dev] = n;
   }
   return g_smem_per_sm[dev];
+}
+
+uint64_t next_call_id() {
+  static std::atomic<uint64_t> counter{
+      static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count()) *
+          0xD1342543DE82EF95ull ^
+      static_cast<uint64_t>(reinterpret_cast<uintptr_t>(&counter))};
+  return counter.fetch_add(0x9E3779B97F4A7C15ull, std::memory_order_relaxed);
 }
 
 int resident_ctas(const void* kernel, int threads, size_t smem) {

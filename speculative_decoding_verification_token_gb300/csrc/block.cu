@@ -317,6 +317,9 @@ static sv_status run_block(const CommonArgs& a, const int64_t* target_row0,
   sp.ws = ws;
   sp.status = status;
   sp.clear_status = stream_clears ? 1 : 0;
+  sp.claim = ws.claim;
+  sp.claim_ready = ws.claim_ready;
+  sp.call_id = next_call_id();
   sp.zero_words = ws.blk.count;  // the two rounds' slot counts
   sp.n_zero = 2;
   profile_mark(0, stream);

@@ -172,6 +172,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
   return true;
 }
 
+// 64-bit global loads with acquire and stores with release semantics at GPU scope.
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // Wait until the request number in shared-memory word `w` reaches `seq`, for at most `limit_ns`;
 // on expiry report SV_ERR_TIMEOUT and give up.
 __device__ __forceinline__ bool wait_seq(const uint32_t* w, uint32_t seq, int32_t* status,

@@ -23,6 +23,10 @@ int device_smem_per_sm();
 // Resident CTAs per SM of `kernel` with `smem` bytes of dynamic shared memory (0 on error).
 int resident_ctas(const void* kernel, int threads, size_t smem);
 
+// A fresh 64-bit value per call, distinct for every call of the process (an odd-stride counter
+// from a time- and address-derived start): tags a launch's own writes in a reused workspace.
+uint64_t next_call_id();
+
 // Diagnostic kernel timing (sv_profile_enable): record event `k` (0..3) on `stream` if enabled.
 void profile_mark(int k, cudaStream_t stream);
 

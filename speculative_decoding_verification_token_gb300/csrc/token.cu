@@ -43,6 +43,9 @@ static sv_status run_token(const CommonArgs& a, const int64_t* target_row0,
   sp.ws = ws;
   sp.status = status;
   sp.clear_status = stream_clears ? 1 : 0;
+  sp.claim = ws.claim;
+  sp.claim_ready = ws.claim_ready;
+  sp.call_id = next_call_id();
   sp.zero_words = nullptr;
   sp.n_zero = 0;
   profile_mark(0, stream);

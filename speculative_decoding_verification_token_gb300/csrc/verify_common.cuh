@@ -58,6 +58,8 @@ struct VerifyWs {
   RaceDesc* desc;    // [B]
   RaceSlot* slots;   // [units]: verify uses B of them, the sampler one per drafted row
   BlockWs blk;
+  int32_t* claim;                   // the stream kernel's item counter
+  unsigned long long* claim_ready;  // the launch's call id once the counter is zeroed
   size_t total;
 };
 
@@ -105,6 +107,8 @@ static inline VerifyWs verify_layout(void* base, int32_t B, int32_t gmax, int64_
   w.blk.done = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * units));
   w.blk.count = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * 2));
   w.blk.rpart = reinterpret_cast<float*>(take(sizeof(float) * 2 * units * size_t(w.blk.CLr)));
+  w.claim = reinterpret_cast<int32_t*>(take(sizeof(int32_t)));
+  w.claim_ready = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long)));
   w.total = off;
   return w;
 }

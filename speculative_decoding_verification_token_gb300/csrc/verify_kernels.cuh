@@ -49,7 +49,14 @@ struct StreamParams {
   int32_t clear_status;  // this launch resets the call's status word (see stream_kernel)
   int32_t* zero_words;   // nullable: counters of the kernels that follow, zeroed by block 0
   int32_t n_zero;
+  int32_t* claim;        // nullable: the tail's item counter (dynamic claims), zeroed by block 0
+  unsigned long long* claim_ready;  // block 0 stores call_id here once the counter is zeroed
+  unsigned long long call_id;       // unique to this launch
 };
+
+// The items of the last kDynRounds rounds are claimed one at a time from a counter instead of
+// dealt out round-robin, so that the SMs that stream faster take more of the tail.
+constexpr int kDynRounds = 2;
 
 struct StageMeta {
   int32_t unit;   // r * gmax + (i - 1); -1 marks the end of the stream
@@ -71,12 +78,40 @@ __device__ void stream_producer(const StreamParams& p, uint8_t* ring, uint64_t* 
   const int64_t n_items = int64_t(p.gmax) * per_pos;
   uint32_t n = 0;      // stages issued so far
   int32_t issued = 0;  // items issued so far
-  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int32_t i = p.gmax - static_cast<int32_t>(item / per_pos);  // highest position first
-    const int64_t rem = item % per_pos;
+  // items [0, n_static) round-robin, the rest claimed; the first claim waits (bounded) until block
+  // 0 has zeroed the counter for this launch
+  const int64_t n_dyn = p.claim ? min(n_items, int64_t(gridDim.x) * kDynRounds) : 0;
+  const int64_t n_static = n_items - n_dyn;
+  bool ready = false;
+  auto next_item = [&](int64_t after) -> int64_t {  // after < 0: this CTA's first item
+    if (after < n_static) {
+      const int64_t s = after < 0 ? int64_t(blockIdx.x) : after + gridDim.x;
+      if (s < n_static) return s;
+    }
+    if (n_dyn == 0) return n_items;
+    if (!ready) {
+      const uint64_t t0 = global_ns();
+      while (ld_acquire_u64(p.claim_ready) != p.call_id) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+          report(p.status, SV_ERR_TIMEOUT);
+          return n_items;
+        }
+        __nanosleep(64);
+      }
+      ready = true;
+    }
+    return n_static + atomicAdd(p.claim, 1);
+  };
+  for (int64_t item = next_item(-1); item < n_items;) {
+    const int64_t cur = item;
+    const int32_t i = p.gmax - static_cast<int32_t>(cur / per_pos);  // highest position first
+    const int64_t rem = cur % per_pos;
     const int32_t r = static_cast<int32_t>(rem / p.C);
     const int32_t c = static_cast<int32_t>(rem % p.C);
-    if (i > clamp_gamma(p.draft_len[r], p.gmax)) continue;  // request r drafted fewer tokens
+    if (i > clamp_gamma(p.draft_len[r], p.gmax)) {  // request r drafted fewer tokens
+      item = next_item(cur);
+      continue;
+    }
     const int32_t unit = r * p.gmax + (i - 1);
     const uint8_t* trow = row_ptr<E>(p.target, p.target_row0[r] + (i - 1), p.ld);
     const uint8_t* drow = row_ptr<E>(p.draft, p.draft_row0[r] + (i - 1), p.ld);
@@ -108,6 +143,7 @@ __device__ void stream_producer(const StreamParams& p, uint8_t* ring, uint64_t* 
       ++n;
     }
     ++issued;
+    item = next_item(cur);  // claimed after this item's copies are under way
   }
   // end-of-stream marker
   const uint32_t stage = n % kRing;
@@ -231,6 +267,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(StreamParams 
     // reports anything, so clearing the word here orders it before every report of the call.
     if (threadIdx.x == 0 && p.clear_status && p.status) *p.status = SV_OK;
     if (threadIdx.x < p.n_zero) p.zero_words[threadIdx.x] = 0;
+    if (threadIdx.x == 0 && p.claim) {  // the counter, then (release) this launch's id
+      *p.claim = 0;
+      st_release_u64(p.claim_ready, p.call_id);
+    }
   }
   __syncthreads();
   if (warp == kConsumerWarps) {

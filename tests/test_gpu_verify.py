@@ -290,3 +290,30 @@ def test_residual_empty_fallback(sv, orc, block, dtype, V):
     assert (kinds[fall] == orc.RACE_RESIDUAL_EMPTY).all(), kinds
     assert (ref["accepted_len"][fall] == fall % 3).all()
     assert res["exempt_mismatch"] == 0
+
+
+@pytest.mark.parametrize("block", [0, 1])
+def test_gpu_emitted_histogram_chisquare_1e6(sv, block):
+    """10^6 independent requests on V = 4, gamma = 2 (fp32), drafts drawn from q by the library's
+    sampler and verified on the GPU: the first emitted token follows p_1 (chi-square, 3 degrees of
+    freedom, the 1e-4 critical value) -- the distribution itself, beside the request-by-request
+    parity with the oracle."""
+    from scipy.special import softmax
+    from scipy.stats import chi2, chisquare
+    V, G, n = 4, 2, 1_000_000
+    rng = np.random.default_rng(2025)
+    T = rng.normal(0, 1.0, (G + 1, V)).astype(np.float32)
+    D = (T[:G] + rng.normal(0, 0.8, (G, V))).astype(np.float32)
+    tgt = torch.from_numpy(np.tile(T, (n, 1))).cuda()
+    drf = torch.from_numpy(np.tile(D, (n, 1))).cuda()
+    tr0 = torch.arange(n, dtype=torch.int64, device="cuda") * (G + 1)
+    dr0 = torch.arange(n, dtype=torch.int64, device="cuda") * G
+    dl = torch.full((n,), G, dtype=torch.int32, device="cuda")
+    toks = sv.spec_sample_draft(drf, dr0, dl, G, 19)
+    fn = sv.spec_verify_block if block else sv.spec_verify_token
+    out = fn(tgt, drf, tr0, dr0, dl, G, toks, 19)
+    torch.cuda.synchronize()
+    assert int(out["status"].item()) == 0
+    counts = np.bincount(out["out_tokens"][:, 0].cpu().numpy(), minlength=V)
+    stat = chisquare(counts, n * softmax(T[0].astype(np.float64))).statistic
+    assert stat < chi2.ppf(1 - 1e-4, V - 1), (counts, stat)

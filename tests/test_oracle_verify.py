@@ -242,3 +242,26 @@ def test_residual_empty_fallback(orc, block):
     keep = p > 0
     stat = chisquare(counts[keep], n * p[keep] / p[keep].sum())
     assert stat.pvalue > 1e-4, (counts, n * p)
+
+
+@pytest.mark.parametrize("block", [0, 1])
+def test_emitted_histogram_chisquare_1e6(orc, block):
+    """10^6 independent requests on V = 4, gamma = 2: drafts drawn from q by the oracle's sampler,
+    verified; the first emitted token follows p_1 (chi-square, 3 degrees of freedom, the 1e-4
+    critical value)."""
+    from scipy.stats import chi2, chisquare
+    V, G, n = 4, 2, 1_000_000
+    rng = np.random.default_rng(2024)
+    T = rng.normal(0, 1.0, (G + 1, V)).astype(np.float32)
+    D = (T[:G] + rng.normal(0, 0.8, (G, V))).astype(np.float32)
+    tgt, drf = np.tile(T, (n, 1)), np.tile(D, (n, 1))
+    tr0 = np.arange(n, dtype=np.int64) * (G + 1)
+    dr0 = np.arange(n, dtype=np.int64) * G
+    dl = np.full(n, G, np.int32)
+    st, toks = orc.sample_draft_batch(drf, V, V, dr0, dl, n, 11)
+    assert st == 0
+    out = orc.verify_batch(block, tgt, drf, V, V, tr0, dr0, dl, toks, n, 11, out_ld=G + 1)
+    assert out["status"] == 0
+    counts = np.bincount(out["out_tokens"][:, 0], minlength=V)
+    stat = chisquare(counts, n * softmax(T[0].astype(np.float64))).statistic
+    assert stat < chi2.ppf(1 - 1e-4, V - 1), (counts, stat)

@@ -742,7 +742,7 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "f32",  # the arithmetic (softmax statistics, ratios, race keys); logits are bf16
         "data": "synthetic",
         "config": token_config(w, world),
         "ms_per_step_median": round(t_med * 1e3, 4),

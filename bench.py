@@ -46,7 +46,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the supplementary rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["markov", "schedule", "block", "lmhead"], default=None,
+    ap.add_argument("--only", choices=["markov", "schedule", "block", "lmhead", "round"],
+                    default=None,
                     help="time one supplementary row alone and print it (profiling runs)")
     ap.add_argument("--markov-positions", type=int, default=None,
                     help="with --only markov: draft this many positions instead of 16")
@@ -415,6 +416,26 @@ def bench_rows(steps, warmup):
     rows["sts_fit_32768x16"] = {"us": sum(t) / len(t) * 1e6, "newton_steps": 30,
                                 "status": int(status.item())}
 
+    rows["scheduled_round_512x16_V129280_bf16"] = bench_round(steps, warmup, flush, stream)
+    rows["markov_draft_256x16_V151936_R256"] = bench_markov(steps, warmup, flush, stream)
+    rows["lmhead_verify_64x5_V151936_H2560_bf16"] = bench_lmhead(steps, warmup, flush, stream)
+    return rows
+
+
+def bench_round(steps, warmup, flush, stream):
+    """A scheduled round: the scheduler over 512 requests x 16 positions, then token verification
+    of the selected prefixes (V = 129280, bf16)."""
+    import torch
+    import speculative_decoding_verification_token_gb300 as sv
+    from speculative_decoding_verification_token_gb300 import synth
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sw = synth.SCHEDULE
+    si = synth.schedule_inputs(sw)
+    c = torch.from_numpy(si["cond_accept"]).to(dev)
+    ml = torch.from_numpy(si["max_len"]).to(dev)
+    sps = torch.from_numpy(si["sps"]).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sws = sv.workspace(sv.dspark_schedule_workspace_bytes(sw.N, sw.K), dev)
     # scheduled round: schedule, then verify the selected prefixes (V = 129280)
     vw = synth.SCHEDULED_VERIFY
     vin = synth.token_inputs(vw, device=dev)
@@ -444,16 +465,13 @@ def bench_rows(steps, warmup):
     n_bonus = int((acc == sel).sum())
     nb = (2 * int(sel.sum()) + n_bonus) * vw.V * 2
     tm = sum(t) / len(t)
-    rows["scheduled_round_512x16_V129280_bf16"] = {
+    row = {
         "ms": tm * 1e3, "GB_s": nb / tm / 1e9, "positions_per_s": int(sel.sum()) / tm,
         "verified_rows": int(rnd["s"]["total_rows"].item()),
         "verify_kernel_ms": {"stream": round(vkms[0], 4), "race_with_decide": round(vkms[2], 4)},
         "status": int(status.item())}
     del vin, vt
-
-    rows["markov_draft_256x16_V151936_R256"] = bench_markov(steps, warmup, flush, stream)
-    rows["lmhead_verify_64x5_V151936_H2560_bf16"] = bench_lmhead(steps, warmup, flush, stream)
-    return rows
+    return row
 
 
 def bench_schedule(steps, warmup):
@@ -711,6 +729,11 @@ def main():
     if args.only == "schedule":
         row = bench_schedule(args.steps, args.warmup)
         print(json.dumps({"row": "schedule", **row}))
+        return
+    if args.only == "round":
+        row = bench_round(args.steps, args.warmup, make_flush(torch.device("cuda")),
+                          torch.cuda.current_stream())
+        print(json.dumps({"row": "scheduled_round", **row}))
         return
     if args.only == "lmhead":
         row = bench_lmhead(args.steps, args.warmup, make_flush(torch.device("cuda")),

@@ -664,30 +664,31 @@ static sv_status launch_race(RaceParams rp, cudaStream_t stream) {
   const int64_t jobs = rp.B;
   if (jobs == 0) return SV_OK;
   rp.CL = race_split(rp.S, jobs);
-  // the kernel's share: ceil(V / (CL * kPer)) whole vectors, staged in shared memory unless that
-  // would leave too few resident CTAs for one wave of every share
+  // the kernel's share: ceil(V / (CL * kPer)) whole vectors, staged in shared memory unless it is
+  // too large, or unless staging would leave too few resident CTAs for one wave of every share
   constexpr int64_t kPer = Elem<E>::kPerVec;
-  const int64_t share_bytes = (rp.V + rp.CL * kPer - 1) / (rp.CL * kPer) * 16;
+  auto share_of = [&](int32_t cl) { return (rp.V + cl * kPer - 1) / (cl * kPer) * 16; };
+  int64_t share_bytes = share_of(rp.CL);
   rp.stage_share = share_bytes <= int64_t(kRaceShareMax);
   const int sms = device_sm_count();
   const int smem_sm = device_smem_per_sm();
-  int64_t stage_bytes = share_bytes;
   if (rp.stage_share && sms > 0 && smem_sm > 0) {
     const int64_t per_sm = std::min<int64_t>(kRaceCtasPerSm, smem_sm / (share_bytes + 4096));
-    if (jobs * rp.CL > int64_t(sms) * per_sm && jobs * rp.CL <= int64_t(sms) * kRaceCtasPerSm) {
-      // the staged shares would not all be resident at once: twice as many shares, half as large
-      // and staged, beat one wave of shares read from global memory (128 jobs of V = 129280
-      // bf16: 0.144 against 0.148 ms per block-verification call)
-      const int32_t cl2 = std::min<int32_t>(std::min<int32_t>(rp.S, kRaceSplitFew), 2 * rp.CL);
-      stage_bytes = (rp.V + cl2 * kPer - 1) / (cl2 * kPer) * 16;
-      if (cl2 > rp.CL && stage_bytes <= int64_t(kRaceShareMax)) {
-        rp.CL = cl2;
-      } else {
-        rp.stage_share = false;
-      }
+    if (jobs * rp.CL > int64_t(sms) * per_sm && jobs * rp.CL <= int64_t(sms) * kRaceCtasPerSm)
+      rp.stage_share = false;
+  }
+  if (!rp.stage_share && sms > 0 && jobs * rp.CL <= int64_t(sms) * kRaceCtasPerSm) {
+    // one wave of shares that cannot all be staged: twice as many shares, half as large (staged
+    // if they fit) beat it -- 128 jobs of V = 129280 bf16, 4 -> 8 shares: 0.148 -> 0.144 ms per
+    // block-verification call; 512 jobs, 1 -> 2 shares: the race of a scheduled round 102 -> 98 us
+    const int32_t cl2 = std::min<int32_t>(std::min<int32_t>(rp.S, kRaceSplitFew), 2 * rp.CL);
+    if (cl2 > rp.CL) {
+      rp.CL = cl2;
+      share_bytes = share_of(cl2);
+      rp.stage_share = share_bytes <= int64_t(kRaceShareMax);
     }
   }
-  const size_t smem = rp.stage_share ? size_t(stage_bytes) : 0;
+  const size_t smem = rp.stage_share ? size_t(share_bytes) : 0;
   if (cudaFuncSetAttribute(race_kernel<E, kBlock>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kRaceShareMax)) != cudaSuccess)
     return SV_ERR_CUDA;

@@ -264,7 +264,8 @@ sv_status spec_verify_shard_finish(const uint64_t* winners_all, int32_t n_shards
  * Two passes over W at most.  The first computes every logit once: the softmax statistics and,
  * per position, the few entries that can win the correction or bonus race; the second recomputes
  * the two rows of only those requests whose candidates cannot prove their winner, and is skipped
- * (an empty launch) when there are none.  The outputs do not depend on which pass settled them.
+ * (an empty launch) when there are none.  Both passes race with the same uniforms, so they draw
+ * the same token unless two keys lie within their rounding of each other.
  * All DEVICE pointers 16-byte aligned; SV_ERR_UNSUPPORTED otherwise, or for V above 2^31 - 256.
  * The workspace (DEVICE, 256-byte aligned) holds a copy of the hidden rows in GEMM order and the
  * per-tile partials: spec_verify_lmhead_workspace_bytes(B, max_draft_len, V, H) bytes, 0 for sizes

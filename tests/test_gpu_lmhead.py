@@ -97,6 +97,14 @@ def test_lmhead_parity_ragged_ids(sv, orc):
     _parity(sv, orc, inp, request_ids=rids)
 
 
+@pytest.mark.parametrize("B,gamma,V,H", [(20, 16, 1500, 64), (7, 2, 200, 192), (33, 3, 777, 128)])
+def test_lmhead_parity_shapes(sv, orc, B, gamma, V, H):
+    """Requests that straddle slot blocks (34 slots per request), one k-block (H = 64), a vocabulary
+    smaller than one tile (V = 200), and an odd vocabulary with odd request counts."""
+    w = synth.LmHeadWorkload("lmhead_shape", B, gamma, V, H, 3.0, 1.1, 1.0, 14 + B, 1013 + B)
+    _parity(sv, orc, synth.lmhead_inputs(w))
+
+
 def test_lmhead_no_drafts(sv, orc):
     """max_draft_len = 0: every request takes its bonus token from target row 0."""
     w = synth.LmHeadWorkload("lmhead_nodraft", 9, 0, 1500, 128, 3.0, 1.1, 1.0, 12, 1010)

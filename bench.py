@@ -75,8 +75,8 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
-def stored_traffic(kernel_key):
-    """Per-launch DRAM bytes of `kernel_key` from profiles/traffic.json if taken on these sources."""
+def stored_counter(kernel_key, field):
+    """A per-launch ncu counter of `kernel_key` (profiles/traffic.json) if taken on these sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -85,7 +85,12 @@ def stored_traffic(kernel_key):
     ent = data.get(kernel_key)
     if not ent or ent.get("source_digest") != source_digest(ent.get("sources", [])):
         return None
-    return ent.get("dram_bytes_per_launch")
+    return ent.get(field)
+
+
+def stored_traffic(kernel_key):
+    """Per-launch DRAM bytes of `kernel_key` from profiles/traffic.json if taken on these sources."""
+    return stored_counter(kernel_key, "dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -609,8 +614,23 @@ def bench_markov(steps, warmup, flush, stream, positions=None):
     peaks, _ = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
     tf = float(peaks["bf16_tflops"])
+    # instruction issue, the bound of the epilogue: warp instructions per position kernel (ncu,
+    # stored with its sources' digest) over the kernel's time, against one warp instruction per
+    # scheduler and clock (152 SMs x 4 schedulers x the maximum SM clock)
+    inst = stored_counter("markov_position_256_V151936_R256", "warp_instructions_per_launch")
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    issue_peak = sms * 4 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    alu = None
+    if inst:
+        achieved = inst / (pos_ms * 1e-3)
+        alu = {"bound": "alu", "achieved": achieved, "peak": issue_peak,
+               "unit": "warp instructions/s", "frac": achieved / issue_peak,
+               "warp_instructions_per_position_kernel": inst,
+               "peak_note": "SMs x 4 schedulers x one warp instruction per clock at the maximum "
+                            "SM clock"}
     return {
         "workload": f"{w.B} requests x {w.K} positions, V={w.V}, R={w.R}, bf16",
+        "alu_roofline": alu,
         "ms": tm * 1e3, "ms_median": statistics.median(t) * 1e3,
         "drafted_positions_per_s": w.B * w.K / tm,
         "algorithmic_bytes_per_call": bytes_call,

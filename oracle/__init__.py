@@ -23,6 +23,7 @@ _lock = threading.Lock()
 _lib = None
 
 TAG_DRAFT, TAG_ACCEPT, TAG_RESID, TAG_BONUS = 0, 1, 2, 3
+TAG_FINE = 4  # added to a race tag: the stream of the low bits of its uniforms
 OK, ERR_ARGS, ERR_TOKEN, ERR_NAN, ERR_ZERO_Q = 0, 1, 2, 3, 4
 RACE_RESIDUAL, RACE_BONUS, RACE_RESIDUAL_EMPTY = 0, 1, 2
 
@@ -63,6 +64,7 @@ def _load():
             "orc_philox4x32_10": (None, [P, P, P]),
             "orc_random_word": (u32, [u64, u64, u32, u32, u64]),
             "orc_uniform": (f64, [u64, u64, u32, u32, u64]),
+            "orc_race_uniform": (f64, [u64, u64, u32, u32, u64]),
             "orc_row_stats": (C.c_int, [P, i64, P, P]),
             "orc_overlap": (f64, [P, P, i64]),
             "orc_expected_words": (f64, [f64, C.c_int]),
@@ -122,6 +124,10 @@ def random_word(seed, req, pos, tag, v):
 
 def uniform(seed, req, pos, tag, v):
     return float(_load().orc_uniform(seed, req, pos, tag, v))
+
+
+def race_uniform(seed, req, pos, tag, v):
+    return float(_load().orc_race_uniform(seed, req, pos, tag, v))
 
 
 # ---- closed forms ----------------------------------------------------------------------------

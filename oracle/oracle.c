@@ -42,12 +42,18 @@ void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t ou
   out[3] = c3;
 }
 
-uint32_t orc_random_word(uint64_t seed, uint64_t req, uint32_t pos, uint32_t tag, uint64_t v) {
+/* The Philox block at counter (group, pos, lo32(req), tag << 24 | hi32(req) & 0xFFFFFF). */
+static void random_block(uint64_t seed, uint64_t req, uint32_t pos, uint32_t tag, uint32_t group,
+                         uint32_t out[4]) {
   uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
-  uint32_t ctr[4] = {(uint32_t)(v >> 2), pos, (uint32_t)(req & 0xFFFFFFFFu),
+  uint32_t ctr[4] = {group, pos, (uint32_t)(req & 0xFFFFFFFFu),
                      (tag << 24) | ((uint32_t)(req >> 32) & 0xFFFFFFu)};
-  uint32_t out[4];
   orc_philox4x32_10(ctr, key, out);
+}
+
+uint32_t orc_random_word(uint64_t seed, uint64_t req, uint32_t pos, uint32_t tag, uint64_t v) {
+  uint32_t out[4];
+  random_block(seed, req, pos, tag, (uint32_t)(v >> 2), out);
   return out[v & 3u];
 }
 
@@ -56,9 +62,19 @@ double orc_uniform(uint64_t seed, uint64_t req, uint32_t pos, uint32_t tag, uint
   return ((double)(w >> 9) + 0.5) * ldexp(1.0, -23);
 }
 
+/* Race entries: 16 high bits from a block shared by 8 entries, 7 low bits from the FINE stream. */
+double orc_race_uniform(uint64_t seed, uint64_t req, uint32_t pos, uint32_t tag, uint64_t v) {
+  uint32_t blk[4];
+  random_block(seed, req, pos, tag, (uint32_t)(v >> 3), blk);
+  uint32_t word = blk[(v >> 1) & 3u];
+  uint32_t h = (v & 1u) ? (word >> 16) : (word & 0xFFFFu);
+  uint32_t f = orc_random_word(seed, req, pos, tag + ORC_TAG_FINE, v) >> 25;
+  return ((double)((h << 7) | f) + 0.5) * ldexp(1.0, -23);
+}
+
 /* -log(E) for the exponential variable E = -log(u) of one race entry. */
 static double race_noise(uint64_t seed, uint64_t req, uint32_t pos, uint32_t tag, uint64_t v) {
-  double u = orc_uniform(seed, req, pos, tag, v);
+  double u = orc_race_uniform(seed, req, pos, tag, v);
   double E = -log(u);
   return -log(E);
 }

@@ -29,7 +29,8 @@
  *   - Logit rows are float arrays (bf16 inputs are widened exactly by the caller); all arithmetic
  *     on them is double.  p = softmax(target row), q = softmax(draft row), temperature 1.
  *   - Positions are 1-based: drafted tokens sit at positions 1..gamma, the bonus row at gamma+1.
- *   - Random uniforms: see orc_uniform().  Tags: DRAFT 0, ACCEPT 1, RESID 2, BONUS 3.
+ *   - Random uniforms: orc_uniform() for scalar draws (the ACCEPT test), orc_race_uniform() for
+ *     the entries of a race.  Tags: DRAFT 0, ACCEPT 1, RESID 2, BONUS 3.
  *   - Exponential race: to sample x with probability w(x)/sum(w), take argmax_x log w(x) - log E_x,
  *     E_x = -log u_x (Exp(1) variables); equal keys resolve to the lowest index; w(x)=0 never wins.
  *
@@ -46,6 +47,9 @@ extern "C" {
 #endif
 
 enum { ORC_TAG_DRAFT = 0, ORC_TAG_ACCEPT = 1, ORC_TAG_RESID = 2, ORC_TAG_BONUS = 3 };
+
+/* Added to a race's tag for the stream that holds the low bits of its uniforms. */
+enum { ORC_TAG_FINE = 4 };
 
 /* Result codes of the oracle calls. */
 enum {
@@ -73,6 +77,14 @@ uint32_t orc_random_word(uint64_t seed, uint64_t req, uint32_t pos, uint32_t tag
 
 /* Uniform in (0,1): u = ((word >> 9) + 0.5) * 2^-23.  Exact in float and double, never 0 or 1. */
 double orc_uniform(uint64_t seed, uint64_t req, uint32_t pos, uint32_t tag, uint64_t v);
+
+/* The uniform of race entry v, on the same grid as orc_uniform (23 bits, n + 0.5 over 2^23):
+ *   n = (h << 7) | f, where
+ *   h = 16-bit half (v & 1) (0: low, 1: high) of word (v >> 1) & 3 of the block at counter
+ *       (v >> 3, pos, lo32(req), (tag << 24) | (hi32(req) & 0xFFFFFF)) -- one block per 8 entries;
+ *   f = orc_random_word(seed, req, pos, tag + ORC_TAG_FINE, v) >> 25.
+ * n is uniform on [0, 2^23) because h and f are independent uniform bit fields. */
+double orc_race_uniform(uint64_t seed, uint64_t req, uint32_t pos, uint32_t tag, uint64_t v);
 
 /* ---- closed forms --------------------------------------------------------------------- */
 

@@ -108,3 +108,60 @@ def test_uniform_stream_statistics(orc):
     # streams of different tags / positions / requests are not shifted copies of each other
     w = np.array([orc.uniform(12345, 77, 2, 3, v) for v in range(2000)])
     assert abs(np.corrcoef(u[:2000], w)[0, 1]) < 0.12
+
+
+def test_race_uniform_layout_matches_library(orc):
+    """Race entry v: n = (h << 7) | f with h the 16-bit half (v & 1) of word (v >> 1) & 3 of the
+    block at counter (v >> 3, pos, lo32(req), tag << 24 | hi32(req)), f the top 7 bits of word v & 3
+    of the block at counter (v >> 2, ...) under tag + 4; u = (n + 0.5) 2^-23.  Both blocks come from
+    the library Philox."""
+    rng = np.random.default_rng(8)
+    cases, meta = [], []
+    for _ in range(4):
+        seed = int(rng.integers(0, 2**64, dtype=np.uint64))
+        ctrs = []
+        for _ in range(16):  # 32 counters: the library kernel takes a power-of-two count
+            req = int(rng.integers(0, 2**56, dtype=np.uint64))
+            pos = int(rng.integers(0, 64))
+            tag = int(rng.choice([orc.TAG_DRAFT, orc.TAG_RESID, orc.TAG_BONUS]))
+            v = int(rng.integers(0, 300000))
+            hi = (req >> 32) & 0xFFFFFF
+            ctrs.append([v >> 3, pos, req & 0xFFFFFFFF, (tag << 24) | hi])
+            ctrs.append([v >> 2, pos, req & 0xFFFFFFFF, ((tag + orc.TAG_FINE) << 24) | hi])
+            meta.append((seed, req, pos, tag, v))
+        cases.append([seed, ctrs])
+    lib = _triton_philox(cases)
+    flat = [w for blk in lib for w in blk]
+    for k, (seed, req, pos, tag, v) in enumerate(meta):
+        coarse, fine = flat[2 * k], flat[2 * k + 1]
+        h = (coarse[(v >> 1) & 3] >> (16 * (v & 1))) & 0xFFFF
+        f = fine[v & 3] >> 25
+        assert orc.race_uniform(seed, req, pos, tag, v) == ((h << 7 | f) + 0.5) * 2.0**-23
+
+
+def test_race_uniform_grid_and_statistics(orc):
+    """Race uniforms lie on the 2^-23 grid inside (0, 1); over a vocabulary-indexed stream the
+    values, their 16 high bits and their 7 low bits are uniform (chi-square), neighbours that share
+    a block are uncorrelated, and the high and low bits are independent (joint chi-square)."""
+    n = 80_000
+    u = np.array([orc.race_uniform(999, 31, 4, orc.TAG_RESID, v) for v in range(n)])
+    assert (u > 0).all() and (u < 1).all()
+    m = u * 2**23 - 0.5
+    assert (m == np.floor(m)).all()
+    m = m.astype(np.int64)
+
+    def chi2(counts):
+        e = counts.sum() / counts.size
+        return ((counts - e) ** 2 / e).sum(), counts.size - 1
+
+    for counts in (np.bincount(m >> 16, minlength=128),          # top 7 bits (coarse part)
+                   np.bincount((m >> 7) & 0xFF, minlength=256),  # low 8 bits of the coarse part
+                   np.bincount(m & 0x7F, minlength=128),         # fine part
+                   np.bincount(((m >> 19) << 3) | (m & 7), minlength=128)):  # joint
+        c2, dof = chi2(counts)
+        assert abs(c2 - dof) < 5 * np.sqrt(2 * dof), (c2, dof)
+    for lag in (1, 2, 7, 8):
+        r = np.corrcoef(u[:-lag], u[lag:])[0, 1]
+        assert abs(r) < 5 / np.sqrt(n), (lag, r)
+    # the low bits are not a copy of the high bits of another entry of the block
+    assert abs(np.corrcoef(m[:-1] & 0x7F, m[1:] >> 16)[0, 1]) < 5 / np.sqrt(n)

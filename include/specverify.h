@@ -28,10 +28,15 @@
  *     pointers 16-byte aligned and ld * sizeof(element) a multiple of 16.  V itself is arbitrary.
  *
  * Random numbers: uniforms come from Philox4x32-10 (Salmon et al., SC'11, "Parallel Random
- * Numbers: As Easy as 1, 2, 3") with key (lo32(seed), hi32(seed)) and counter
- * (v >> 2, position, lo32(request id), tag << 24 | (hi32(request id) & 0xFFFFFF)), word v & 3,
- * converted as u = ((word >> 9) + 0.5) * 2^-23 (never 0 or 1).  Tags: DRAFT 0, ACCEPT 1, RESID 2,
- * BONUS 3.  Positions are 1-based: drafted tokens at 1..gamma, the bonus row at gamma + 1.
+ * Numbers: As Easy as 1, 2, 3") with key (lo32(seed), hi32(seed)); block(g, tag) is the output
+ * for counter (g, position, lo32(request id), tag << 24 | (hi32(request id) & 0xFFFFFF)).
+ * Every uniform is u = (n + 0.5) * 2^-23 for a 23-bit n (never 0 or 1):
+ *   - the ACCEPT draw of a position: n = word 0 of block(0, ACCEPT) >> 9;
+ *   - race entry v (vocabulary index) under tag T: n = (h << 7) | f, with h the 16-bit half v & 1
+ *     (0: low) of word (v >> 1) & 3 of block(v >> 3, T) -- one block per 8 entries -- and f the
+ *     top 7 bits of word v & 3 of block(v >> 2, T + 4).
+ * Tags: DRAFT 0, ACCEPT 1, RESID 2, BONUS 3.  Positions are 1-based: drafted tokens at 1..gamma,
+ * the bonus row at gamma + 1.
  * Every sample is an exponential race: x = argmax_x log w(x) - log(-log u_x), which draws x with
  * probability w(x) / sum(w) without a normalisation pass; equal keys go to the lower index.
  *

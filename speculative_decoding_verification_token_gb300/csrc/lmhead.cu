@@ -179,12 +179,12 @@ __device__ __forceinline__ void offer_key(float k, int32_t e, KeyIdx& b) {
   }
 }
 
-// Exact keys of entry e (logits t, d; Philox word w): the race's own key into `best` (residual or
+// Exact keys of entry e (logits t, d; race uniform u): the race's own key into `best` (residual or
 // bonus), and for a residual race the key of the race over p with the same uniform into `fb`.
-__device__ __forceinline__ void key_entry(const RaceSpec& rs, float t, float d, uint32_t w,
+__device__ __forceinline__ void key_entry(const RaceSpec& rs, float t, float d, float u,
                                           int32_t e, KeyIdx& best, KeyIdx& fb) {
   if (!(t > -INFINITY)) return;
-  const float noise = race_noise(uniform_of(w));
+  const float noise = race_noise(u);
   if (rs.resid) offer_key(t + noise, e, fb);
   if (race_active(rs, t, d)) offer_key(race_key(rs, t, d, noise), e, best);
 }
@@ -234,25 +234,44 @@ __device__ __forceinline__ void cand_insert(CandList& c, float a, float b, int32
 
 // Offers 16 entries (columns e0 .. e0 + 15, e0 a multiple of 16) with target logits tt and draft
 // logits dd, against the gate key G: an entry enters the list only if its plain key exceeds both
-// the list's smallest key and G.  Its logit must then be within kMaxNoise of that bound, and its
-// Philox word must pass the noise gate of race.cuh; the few entries that pass are keyed exactly.
+// the list's smallest key and G.  Its logit must then be within kMaxNoise of that bound, and the
+// coarse half of its uniform must pass the noise gate of race.cuh (first for each 8 entries at
+// once, on their coarse block's largest half); the few entries that pass are collected in a mask
+// and keyed exactly afterwards, drawing their low bits in one (not unrolled) loop.
 __device__ __forceinline__ void cand_offer16(CandList& c, const Stream& st, const float* tt,
                                              const float* dd, int64_t e0, float G) {
 #pragma unroll
-  for (int g4 = 0; g4 < 4; ++g4) {
+  for (int g8 = 0; g8 < 2; ++g8) {
     const float T = fmaxf(c.amin, G);
-    const float tm = fmaxf(fmaxf(tt[4 * g4], tt[4 * g4 + 1]), fmaxf(tt[4 * g4 + 2], tt[4 * g4 + 3]));
+    float tm = tt[8 * g8];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) tm = fmaxf(tm, tt[8 * g8 + q]);
     if (!(tm >= T - kMaxNoise)) continue;
     const float cg = 23.0f - T * kLog2e;
-    const uint4 blk = stream_block(st, static_cast<uint32_t>((e0 >> 2) + g4));
-    const uint32_t w4[4] = {blk.x, blk.y, blk.z, blk.w};
+    const uint4 blk = stream_block(st, static_cast<uint32_t>((e0 >> 3) + g8));
+    if (gate_mh(half_max(blk)) > gate_threshold(tm, cg)) continue;
+    uint32_t surv = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float t = tt[4 * g4 + q];
-      if (!(t > -INFINITY) || !(gate_m(w4[q]) <= gate_threshold(t, cg))) continue;
-      const float a = t + race_noise(uniform_of(w4[q]));
-      if (a > c.amin && a > G)
-        cand_insert(c, a, dd[4 * g4 + q] - t, static_cast<int32_t>(e0 + 4 * g4 + q));
+    for (int q = 0; q < 8; ++q) {
+      const float t = tt[8 * g8 + q];
+      const uint32_t hq = half_of(blk, static_cast<uint32_t>(q));
+      if (t > -INFINITY && gate_mh(hq) <= gate_threshold(t, cg)) surv |= 1u << q;
+    }
+#pragma unroll 1
+    while (surv) {
+      const uint32_t q = __ffs(surv) - 1;
+      surv &= surv - 1;
+      float t = 0.f, d = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (uint32_t(k) == q) {
+          t = tt[8 * g8 + k];
+          d = dd[8 * g8 + k];
+        }
+      const int64_t e = e0 + 8 * g8 + q;
+      const float u = race_uniform_at(st, static_cast<uint64_t>(e), half_of(blk, q));
+      const float a = t + race_noise(u);
+      if (a > c.amin && a > G) cand_insert(c, a, d - t, static_cast<int32_t>(e));
     }
   }
 }
@@ -654,30 +673,35 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             }
           if (tm > -INFINITY) {
             const int64_t e = e0 + cm;
-            const uint4 b = stream_block(rs.st, static_cast<uint32_t>(e >> 2));
-            key_entry(rs, tm, dm, word_of(b, static_cast<uint32_t>(e & 3)),
+            const uint4 b = stream_block(rs.st, static_cast<uint32_t>(e >> 3));
+            const uint32_t hm = half_of(b, static_cast<uint32_t>(e & 7));
+            key_entry(rs, tm, dm, race_uniform_at(rs.st, static_cast<uint64_t>(e), hm),
                       static_cast<int32_t>(e), best, fb);
             seeded = true;
           }
         }
         // gate (race.cuh): an entry reaches the bound K only if its logit is within kMaxNoise
-        // of K and its Philox word passes the noise threshold; the survivors are keyed exactly
+        // of K and the coarse half of its uniform passes the noise threshold (first for 8
+        // entries at once); the survivors draw their low bits and are keyed exactly
         const float K = fmaxf(best.key, key_from_order(kpub));
         const float floor_t = K - kMaxNoise;
         const float cg = 23.0f - K * kLog2e;
 #pragma unroll
-        for (int g4 = 0; g4 < kHalf / 4; ++g4) {
-          const float tm = fmaxf(fmaxf(tt[4 * g4], tt[4 * g4 + 1]),
-                                 fmaxf(tt[4 * g4 + 2], tt[4 * g4 + 3]));
-          if (!(tm >= floor_t)) continue;
-          const uint4 b = stream_block(rs.st, static_cast<uint32_t>((e0 >> 2) + g4));
-          const uint32_t w4[4] = {b.x, b.y, b.z, b.w};
+        for (int g8 = 0; g8 < kHalf / 8; ++g8) {
+          float tm = tt[8 * g8];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float tv = tt[4 * g4 + c];
-            if (!(gate_m(w4[c]) <= gate_threshold(tv, cg))) continue;
-            key_entry(rs, tv, dd[4 * g4 + c], w4[c], static_cast<int32_t>(e0 + 4 * g4 + c),
-                      best, fb);
+          for (int c = 1; c < 8; ++c) tm = fmaxf(tm, tt[8 * g8 + c]);
+          if (!(tm >= floor_t)) continue;
+          const uint4 b = stream_block(rs.st, static_cast<uint32_t>((e0 >> 3) + g8));
+          if (gate_mh(half_max(b)) > gate_threshold(tm, cg)) continue;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float tv = tt[8 * g8 + c];
+            const uint32_t hv = half_of(b, static_cast<uint32_t>(c));
+            if (!(gate_mh(hv) <= gate_threshold(tv, cg))) continue;
+            const int64_t e = e0 + 8 * g8 + c;
+            key_entry(rs, tv, dd[8 * g8 + c], race_uniform_at(rs.st, static_cast<uint64_t>(e), hv),
+                      static_cast<int32_t>(e), best, fb);
           }
         }
         const float kp = key_from_order(kpub);

@@ -97,8 +97,10 @@ __device__ __noinline__ KeyIdx markov_survivors(Stream st, uint32_t surv, int64_
         *reinterpret_cast<const uint16_t*>(tile + tc::sw128(r, cq + (j >> 3)) + 2 * (j & 7));
     const float z = __uint_as_float(uint32_t(zbits) << 16);
     if (!(z > -INFINITY)) continue;
-    const uint4 blk = stream_block(st, static_cast<uint32_t>(e >> 2));
-    const float key = z + race_noise(uniform_of(word_of(blk, j & 3)));
+    const uint4 blk = stream_block(st, static_cast<uint32_t>(e >> 3));
+    const float u = race_uniform_at(st, static_cast<uint64_t>(e),
+                                    half_of(blk, static_cast<uint32_t>(e & 7)));
+    const float key = z + race_noise(u);
     if (race_better(key, static_cast<int32_t>(e), best.key, best.idx)) {
       best.key = key;
       best.idx = static_cast<int32_t>(e);
@@ -342,10 +344,12 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         s += t.x + t.y;
       }
       // exponential race, key z_j + G_j with G_j = -log(-log u_j).  K is the larger of this
-      // thread's best key and the row bound.  Entry j can reach K only if G_j >= K - z_j; since G <= -log(1 - u) and
-      // 1 - u > ((~w) >> 9) 2^-23, that needs ((~w) >> 9) <= 2^((z_j - K) log2e + 23)
+      // thread's best key and the row bound.  Entry j can reach K only if G_j >= K - z_j; since
+      // G <= -log(1 - u) and 1 - u > m_j 2^-23 with m_j >= (0xFFFF - h_j) << 7 for the coarse half
+      // h_j of u_j, that needs (0xFFFF - h_j) << 7 <= 2^((z_j - K) log2e + 23)
       // = e_j 2^(m2 + 23 - K log2e).  The 1e-3 margin covers the binary32 rounding of both
-      // sides; the few entries that pass are keyed exactly (markov_survivors).
+      // sides; the few entries that pass draw their low bits and are keyed exactly
+      // (markov_survivors).  The 16 columns' coarse halves are two Philox blocks.
       {
         if (best.idx < 0 && tmax > -INFINITY) {
           // first finite tile: seed K with the exact key of the tile's largest z
@@ -357,21 +361,23 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         const float kp = key_from_order(kpub);
         const float K = fmaxf(best.key, kp);
         const float C = fast_exp2(m2 + 23.0f - K * kLog2e) * 1.001f;
-        // rej collects, most significant first, the sign of e_j C - ((~w) >> 9): set = rejected
-        // (fma rounds the exact difference once, so its sign is exact)
+        // rej collects, most significant first, the sign of e_j C - ((0xFFFF - h_j) << 7):
+        // set = rejected (fma rounds the exact difference once, so its sign is exact)
         uint32_t rej = 0;
         const float2 C2 = splat2(C);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const uint4 blk = stream_block(st, static_cast<uint32_t>((c0 >> 2) + g));
+        for (int g = 0; g < 2; ++g) {
+          const uint4 blk = stream_block(st, static_cast<uint32_t>((c0 >> 3) + g));
           const uint32_t w4[4] = {blk.x, blk.y, blk.z, blk.w};
 #pragma unroll
-          for (int j = 0; j < 4; j += 2) {
-            // -((~w) >> 9) as binary32, for two entries: -(2^23 + that integer), plus 2^23
-            const float2 nmf = add2(make_float2(__uint_as_float((w4[j] >> 9) ^ 0xCB7FFFFFu),
-                                                __uint_as_float((w4[j + 1] >> 9) ^ 0xCB7FFFFFu)),
-                                    splat2(8388608.0f));
-            const float2 d = fma2(e[2 * g + j / 2], C2, nmf);
+          for (int k = 0; k < 4; ++k) {
+            // entries 8g + 2k (low half) and 8g + 2k + 1 (high half): -((0xFFFF - h) << 7) as
+            // binary32, from -(2^23 + that integer) plus 2^23
+            const float2 nmf =
+                add2(make_float2(__uint_as_float(((w4[k] & 0xFFFFu) << 7) ^ 0xCB7FFF80u),
+                                 __uint_as_float(((w4[k] >> 9) & 0x7FFF80u) ^ 0xCB7FFF80u)),
+                     splat2(8388608.0f));
+            const float2 d = fma2(e[4 * g + k], C2, nmf);
             rej = __funnelshift_l(__float_as_uint(d.x), rej, 1);
             rej = __funnelshift_l(__float_as_uint(d.y), rej, 1);
           }

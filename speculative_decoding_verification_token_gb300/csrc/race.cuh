@@ -12,9 +12,10 @@
 //         the best that the job's other shares have published, is a lower bound K0 on the winning
 //         key;
 //   main  an entry can reach K0 only if its logit is within kMaxNoise of K0 (no uniform needed to
-//         reject the rest) and, given its uniform, only if its noise reaches K0 - t (the noise gate,
-//         tested for a whole 16-byte vector at once on its largest Philox word); the entries of the
-//         few vectors that pass are gated one by one and keyed exactly.
+//         reject the rest) and, given the 16 high bits of its uniform, only if its noise can reach
+//         K0 - t (the noise gate, tested for a whole 16-byte vector at once on the largest coarse
+//         half of its block); the entries of the few vectors that pass are gated one by one, and
+//         those that pass draw their low bits and are keyed exactly.
 #pragma once
 
 #include "sv_device.cuh"
@@ -49,15 +50,23 @@ __device__ __forceinline__ bool race_active(const RaceSpec& rs, float t, float d
   return rs.resid ? ((d - t) + rs.gap < 0.f) : (t > -INFINITY);
 }
 
-// Exact key of vocabulary entry e with logit t, or -inf if the entry carries no weight (reads the
-// draft logit of a residual entry; used on the rare survivors only).
+// Exact key of vocabulary entry e with logit t and coarse half h, or -inf if the entry carries no
+// weight (reads the draft logit of a residual entry; used on the rare survivors only).
+template <typename E>
+__device__ __noinline__ float exact_key_h(const RaceSpec& rs, float t, const uint8_t* drow,
+                                          int64_t e, uint32_t h) {
+  const float d = rs.resid ? Elem<E>::load(drow, e) : 0.f;
+  if (!race_active(rs, t, d)) return -INFINITY;
+  return race_key(rs, t, d, race_noise(race_uniform_at(rs.st, uint64_t(e + rs.off), h)));
+}
+
+// The same, drawing the coarse half too.
 template <typename E>
 __device__ __noinline__ float exact_key_t(const RaceSpec& rs, float t, const uint8_t* drow,
                                           int64_t e) {
-  const float d = rs.resid ? Elem<E>::load(drow, e) : 0.f;
-  if (!race_active(rs, t, d)) return -INFINITY;
-  const uint4 b = stream_block(rs.st, static_cast<uint32_t>((e + rs.off) >> 2));
-  return race_key(rs, t, d, race_noise(uniform_of(word_of(b, static_cast<uint32_t>(e & 3)))));
+  const uint64_t v = uint64_t(e + rs.off);
+  const uint4 b = stream_block(rs.st, static_cast<uint32_t>(v >> 3));
+  return exact_key_h<E>(rs, t, drow, e, half_of(b, static_cast<uint32_t>(v & 7)));
 }
 
 template <typename E>
@@ -112,17 +121,14 @@ __device__ __forceinline__ float vec_max<float>(const uint4& v) {
 }
 
 // Noise gate.  key <= t + G with G = -log(-log u) <= -log(1 - u), and 1 - u > m 2^-23 with
-// m = (~w) >> 9 = 0x7FFFFF - (w >> 9).  So an entry reaches the bound K only if
-// m <= 2^23 e^(t - K) = 2^(t log2e + c), c = 23 - K log2e.  A whole vector can hold such an
-// entry only if its smallest m -- that of its largest Philox word -- is within the threshold of its
-// largest logit: one integer max per entry and one ex2 per vector reject almost every vector.  The
-// factor 1.001 covers the binary32 rounding of the threshold and of the keys.
+// m = 0x7FFFFF - n for the uniform's 23-bit numerator n.  So an entry reaches the bound K only if
+// m <= 2^23 e^(t - K) = 2^(t log2e + c), c = 23 - K log2e.  The coarse half h bounds m from
+// below by gate_mh(h) whatever the low bits, so a whole 8-entry vector can hold such an entry only
+// if gate_mh of its block's largest half is within the threshold of its largest logit: one Philox
+// block, three SIMD maxima and one ex2 per vector reject almost every vector.  The factor 1.001
+// covers the binary32 rounding of the threshold and of the keys.
 __device__ __forceinline__ float gate_threshold(float t, float c) {
   return fast_exp2(fmaf(t, kLog2e, c)) * 1.001f;
-}
-
-__device__ __forceinline__ float gate_m(uint32_t w) {
-  return static_cast<float>(0x7FFFFFu - (w >> 9));  // exact: below 2^23
 }
 
 constexpr int kSeedBatch = 8;  // vectors whose loads each thread issues before using any (seed)
@@ -175,13 +181,13 @@ __device__ __forceinline__ float seed_range(const RaceSpec& rs, const uint4* vsr
   return be >= 0 ? exact_key_t<E>(rs, bt, drow, be) : -INFINITY;
 }
 
-// Offers entry e, with logit t and Philox word w, to the race if it passes the gate.
+// Offers entry e, with logit t and coarse half h, to the race if it passes the gate.
 template <typename E>
 __device__ __forceinline__ void offer(const RaceSpec& rs, const uint8_t* trow,
-                                      const uint8_t* drow, int64_t e, float t, uint32_t w,
+                                      const uint8_t* drow, int64_t e, float t, uint32_t h,
                                       float c, float& bk, int32_t& bi) {
-  if (!(gate_m(w) <= gate_threshold(t, c))) return;
-  const float k = exact_key_t<E>(rs, t, drow, e);
+  if (!(gate_mh(h) <= gate_threshold(t, c))) return;
+  const float k = exact_key_h<E>(rs, t, drow, e, h);
   if (k > -INFINITY && race_better(k, int32_t(e), bk, bi)) {
     bk = k;
     bi = int32_t(e);
@@ -212,26 +218,29 @@ __device__ __forceinline__ void race_range(const RaceSpec& rs, const uint4* vsrc
       const int64_t e = e0 + int64_t(v) * kPer;
       const float tmax = vec_max<E>(a[u]);
       if (!(tmax >= floor_t)) continue;
-      // e is a multiple of kPer (>= 4): the vector's words are whole Philox blocks
-      const uint4 b0 = stream_block(rs.st, static_cast<uint32_t>((e + rs.off) >> 2));
-      const uint4 b1 =
-          kPer == 8 ? stream_block(rs.st, static_cast<uint32_t>((e + rs.off) >> 2) + 1) : b0;
-      const uint32_t wmax = max(max(max(b0.x, b0.y), max(b0.z, b0.w)),
-                                max(max(b1.x, b1.y), max(b1.z, b1.w)));
-      if (gate_m(wmax) > gate_threshold(tmax, c)) continue;
+      // e + off is a multiple of kPer (8 or 4): the vector's halves are one coarse block (8) or
+      // its first or second pair of words (4)
+      const uint64_t g = uint64_t(e + rs.off);
+      uint4 b = stream_block(rs.st, static_cast<uint32_t>(g >> 3));
+      if (kPer == 4) {
+        const bool upper = (g & 4) != 0;
+        b = make_uint4(upper ? b.z : b.x, upper ? b.w : b.y, 0u, 0u);
+      }
+      if (gate_mh(half_max(b)) > gate_threshold(tmax, c)) continue;
       float x[8];
       Elem<E>::unpack(a[u], x);
-      const uint32_t w[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int q = 0; q < kPer; ++q) offer<E>(rs, trow, drow, e + q, x[q], w[q], c, bk, bi);
+      for (int q = 0; q < kPer; ++q)
+        offer<E>(rs, trow, drow, e + q, x[q], half_of(b, uint32_t(q)), c, bk, bi);
     }
   }
   for (int i = nvec * kPer + threadIdx.x; i < len; i += kThreads) {
     const int64_t e = e0 + i;
     const float x = Elem<E>::load(trow, e);
     if (!(x >= floor_t)) continue;
-    const uint4 b = stream_block(rs.st, static_cast<uint32_t>((e + rs.off) >> 2));
-    offer<E>(rs, trow, drow, e, x, word_of(b, static_cast<uint32_t>(e & 3)), c, bk, bi);
+    const uint64_t g = uint64_t(e + rs.off);
+    const uint4 b = stream_block(rs.st, static_cast<uint32_t>(g >> 3));
+    offer<E>(rs, trow, drow, e, x, half_of(b, static_cast<uint32_t>(g & 7)), c, bk, bi);
   }
 }
 

@@ -23,6 +23,9 @@ constexpr float kMaxNoise = 16.75f;
 
 enum : uint32_t { kTagDraft = 0, kTagAccept = 1, kTagResid = 2, kTagBonus = 3 };
 
+// Added to a race's tag for the stream that holds the low bits of its entries' uniforms.
+constexpr uint32_t kTagFine = 4;
+
 // ---- Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11, "Parallel Random Numbers: As Easy as
 // 1, 2, 3", section 3.3): ten rounds of the 4x32 S-box; the round multipliers act on words 0 and
 // 2, their high halves are xored with the odd words and the round key, and the key advances by the
@@ -68,6 +71,44 @@ __device__ __forceinline__ uint32_t word_of(const uint4& b, uint32_t lane) {
 // u = ((w >> 9) + 1/2) * 2^-23, exact in binary32, inside (0, 1).
 __device__ __forceinline__ float uniform_of(uint32_t w) {
   return (static_cast<float>(w >> 9) + 0.5f) * 1.1920928955078125e-07f;
+}
+
+// Race entries.  The uniform of vocabulary entry v is (n + 1/2) 2^-23 with n = (h << 7) | f:
+//   h = 16-bit half (v & 1) (0: low) of word (v >> 1) & 3 of the block at counter v >> 3, so one
+//       block serves 8 consecutive entries (the block at v >> 3 is the race's coarse block);
+//   f = the top 7 bits of word v & 3 of the block at counter v >> 2 of the FINE stream (tag + 4),
+//       drawn only for the few entries whose coarse half does not settle the noise gate.
+__device__ __forceinline__ uint32_t half_of(const uint4& b, uint32_t j) {
+  const uint32_t w = word_of(b, j >> 1);
+  return (j & 1u) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+__device__ __forceinline__ Stream fine_stream(Stream s) {
+  s.hi += kTagFine << 24;
+  return s;
+}
+
+// u = (((h << 7) | (fine_word >> 25)) + 1/2) * 2^-23, exact in binary32, inside (0, 1).
+__device__ __forceinline__ float race_uniform(uint32_t h, uint32_t fine_word) {
+  return (static_cast<float>((h << 7) | (fine_word >> 25)) + 0.5f) * 1.1920928955078125e-07f;
+}
+
+// The uniform of race entry v whose coarse half h is known: one FINE block.
+__device__ __forceinline__ float race_uniform_at(const Stream& s, uint64_t v, uint32_t h) {
+  const uint4 fb = stream_block(fine_stream(s), static_cast<uint32_t>(v >> 2));
+  return race_uniform(h, word_of(fb, static_cast<uint32_t>(v & 3)));
+}
+
+// The largest of the 8 coarse halves of a block (SIMD 16-bit maxima).
+__device__ __forceinline__ uint32_t half_max(const uint4& b) {
+  const uint32_t m = __vmaxu2(__vmaxu2(b.x, b.y), __vmaxu2(b.z, b.w));
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+// Lower bound on m = 2^23 (1 - u) - 1/2 = 0x7FFFFF - n over the 128 uniforms that share the
+// coarse half h: (0xFFFF - h) << 7, exact in binary32.
+__device__ __forceinline__ float gate_mh(uint32_t h) {
+  return static_cast<float>((0xFFFFu - h) << 7);
 }
 
 // -log(E) with E = -log(u) the exponential variable of a race entry.  Accurate logf: race winners

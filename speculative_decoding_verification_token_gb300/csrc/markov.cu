@@ -361,14 +361,19 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         const float kp = key_from_order(kpub);
         const float K = fmaxf(best.key, kp);
         const float C = fast_exp2(m2 + 23.0f - K * kLog2e) * 1.001f;
-        // rej collects, most significant first, the sign of e_j C - ((0xFFFF - h_j) << 7):
-        // set = rejected (fma rounds the exact difference once, so its sign is exact)
-        uint32_t rej = 0;
+        // First per block of 8 entries: the largest coarse half against the largest e_j C
+        // rejects almost every block.  Within a block that passes, rej collects, most
+        // significant first, the sign of e_j C - ((0xFFFF - h_j) << 7): set = rejected (fma
+        // rounds the exact difference once, so its sign is exact).
+        uint32_t surv = 0;  // bit j: entry j may beat K
         const float2 C2 = splat2(C);
+        const float ecap = fast_exp2(vm - m2) * 1.001f * C;  // >= e_j C for each of the 16
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const uint4 blk = stream_block(st, static_cast<uint32_t>((c0 >> 3) + g));
+          if (gate_mh(half_max(blk)) > ecap) continue;  // none of the block's 8 entries passes
           const uint32_t w4[4] = {blk.x, blk.y, blk.z, blk.w};
+          uint32_t rej = 0;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             // entries 8g + 2k (low half) and 8g + 2k + 1 (high half): -((0xFFFF - h) << 7) as
@@ -381,8 +386,8 @@ __global__ void __launch_bounds__(kMkThreads, 1)
             rej = __funnelshift_l(__float_as_uint(d.x), rej, 1);
             rej = __funnelshift_l(__float_as_uint(d.y), rej, 1);
           }
+          surv |= (__brev(~rej) >> 24) << (8 * g);
         }
-        const uint32_t surv = __brev(~rej) >> 16;  // bit j: entry j may beat K
         if (surv) best = markov_survivors(st, surv, c0, p.V, zt, lane, 2 * h, best);
         if (kslot) {
           if (best.key > published && best.key > kp) {

@@ -157,6 +157,24 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   const int32_t m0 = mb * kMkRows;
   const int32_t n_my = ci < p.n_tiles ? (p.n_tiles - ci + p.per_mblock - 1) / p.per_mblock : 0;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Wt and backbone tiles of tile t into ring stage t % kMkStages (producer thread only).  Wt is
+  // read again at every position and by both M-blocks: keep it in L2 ahead of the backbone, which
+  // is read once.
+  auto issue_wt = [&](int t) {
+    const int32_t n = ci + t * p.per_mblock;
+    const int s = t % kMkStages;
+    mbar_expect_tx(&b_full[s], kMkBBytes);
+    for (int kb = 0; kb < kMkKB; ++kb)
+      tc::tma_load_2d_hint(sB + s * kMkBBytes + kb * (kMkCols * 128), &map_wt, kb * 64,
+                           n * kMkCols, &b_full[s], tc::policy_evict_last());
+  };
+  auto issue_bb = [&](int t) {
+    const int32_t n = ci + t * p.per_mblock;
+    const int s = t % kMkStages;
+    mbar_expect_tx(&bb_full[s], kMkBBBytes);
+    tc::tma_load_3d_hint(sBB + s * kMkBBBytes, &map_bb, n * kMkCols, p.k - 1, m0, &bb_full[s],
+                         tc::policy_evict_first());
+  };
 
   if (tid == 0) {
     s_bad = 0;
@@ -175,6 +193,12 @@ __global__ void __launch_bounds__(kMkThreads, 1)
       mbar_init(&z_empty[z], 1);
     }
     fence_barrier_init();
+    // The first stages hold Wt and backbone tiles, which no kernel of this call writes: they are
+    // requested before the wait for the previous position's tokens
+    for (int t = 0; t < kMkStages && t < n_my; ++t) {
+      issue_wt(t);
+      issue_bb(t);
+    }
   }
   if (warp == 1) tc::tmem_alloc(&tmem_base, kMkTmemCols);
   // A programmatic dependent of the previous position's select kernel: x_{k-1} and the partials
@@ -211,22 +235,13 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   if (warp == 0) {
     // ---- producer
     if (lane == 0) {
-      // Wt is read again at every position and by both M-blocks: keep it in L2 ahead of the
-      // backbone, which is read once
-      const uint64_t keep = tc::policy_evict_last(), once = tc::policy_evict_first();
-      for (int t = 0; t < n_my; ++t) {
-        const int32_t n = ci + t * p.per_mblock;
+      for (int t = kMkStages; t < n_my; ++t) {  // tiles 0 .. kMkStages - 1 were issued above
         const int s = t % kMkStages;
         const uint32_t use = t / kMkStages;
-        if (t >= kMkStages && !mbar_wait(&b_empty[s], (use - 1) & 1, p.status)) break;
-        mbar_expect_tx(&b_full[s], kMkBBytes);
-        for (int kb = 0; kb < kMkKB; ++kb)
-          tc::tma_load_2d_hint(sB + s * kMkBBytes + kb * (kMkCols * 128), &map_wt, kb * 64,
-                               n * kMkCols, &b_full[s], keep);
-        if (t >= kMkStages && !mbar_wait(&bb_empty[s], (use - 1) & 1, p.status)) break;
-        mbar_expect_tx(&bb_full[s], kMkBBBytes);
-        tc::tma_load_3d_hint(sBB + s * kMkBBBytes, &map_bb, n * kMkCols, p.k - 1, m0, &bb_full[s],
-                             once);
+        if (!mbar_wait(&b_empty[s], (use - 1) & 1, p.status)) break;
+        issue_wt(t);
+        if (!mbar_wait(&bb_empty[s], (use - 1) & 1, p.status)) break;
+        issue_bb(t);
       }
     }
   } else if (warp == 1) {

@@ -317,3 +317,27 @@ def test_gpu_emitted_histogram_chisquare_1e6(sv, block):
     counts = np.bincount(out["out_tokens"][:, 0].cpu().numpy(), minlength=V)
     stat = chisquare(counts, n * softmax(T[0].astype(np.float64))).statistic
     assert stat < chi2.ppf(1 - 1e-4, V - 1), (counts, stat)
+
+
+@pytest.mark.parametrize("dtype,V", [(torch.bfloat16, 3001), (torch.float32, 2999)])
+def test_flat_rows_sample_the_largest_race_uniform(sv, orc, dtype, V):
+    """Rows of equal logits: every key is one constant plus the noise of its race uniform, so the
+    sampler must return the entry of largest uniform -- the oracle's race_uniform, evaluated entry
+    by entry -- for each drafted row.  Exercises the coarse-half gate where every entry is within
+    reach of the bound, the FINE blocks, the ragged tail (V not a multiple of 8) and request ids
+    with high bits."""
+    B, G, seed = 5, 3, 2024
+    rids = np.array([7, 2**33 + 1, 2**47 + 12345, 0, 99], dtype=np.uint64)
+    ld = (V + 7) // 8 * 8  # row starts 16-byte aligned
+    drf = torch.zeros((B * G, ld), dtype=dtype, device="cuda")[:, :V]
+    dr0 = torch.arange(B, dtype=torch.int64, device="cuda") * G
+    dl = torch.full((B,), G, dtype=torch.int32, device="cuda")
+    toks = sv.spec_sample_draft(drf, dr0, dl, G, seed,
+                                request_ids=torch.from_numpy(rids.view(np.int64)).cuda())
+    torch.cuda.synchronize()
+    toks = toks.cpu().numpy()
+    for r in range(B):
+        for i in range(G):
+            u = np.array([orc.race_uniform(seed, int(rids[r]), i + 1, orc.TAG_DRAFT, v)
+                          for v in range(V)])
+            assert toks[r * G + i] == int(np.argmax(u)), (r, i)

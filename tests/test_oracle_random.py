@@ -165,3 +165,18 @@ def test_race_uniform_grid_and_statistics(orc):
         assert abs(r) < 5 / np.sqrt(n), (lag, r)
     # the low bits are not a copy of the high bits of another entry of the block
     assert abs(np.corrcoef(m[:-1] & 0x7F, m[1:] >> 16)[0, 1]) < 5 / np.sqrt(n)
+
+
+def _argmax_race_uniform(orc, seed, req, pos, tag, V):
+    u = np.array([orc.race_uniform(seed, req, pos, tag, v) for v in range(V)])
+    return int(np.argmax(u))  # the first of equal maxima: equal keys go to the lowest index
+
+
+def test_flat_row_race_picks_largest_uniform(orc):
+    """On a row of equal logits every key is the same constant plus -log(-log u), increasing in u:
+    the race must return the entry of largest race uniform (the lowest index among equal ones)."""
+    for req, pos, tag, V in ((3, 1, orc.TAG_DRAFT, 2999), (2**40 + 7, 4, orc.TAG_BONUS, 1024),
+                             (11, 2, orc.TAG_RESID, 77)):
+        st, tok, _ = orc.sample_race(np.zeros(V, np.float32), 515, req, pos, tag)
+        assert st == 0
+        assert tok == _argmax_race_uniform(orc, 515, req, pos, tag, V)

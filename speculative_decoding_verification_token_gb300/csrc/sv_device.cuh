@@ -43,8 +43,9 @@ __device__ __forceinline__ uint4 philox_block(uint4 c, uint32_t k0, uint32_t k1)
   return c;
 }
 
-// One stream of uniforms: key (lo32(seed), hi32(seed)); counter (v >> 2, pos, lo32(req),
-// tag << 24 | hi32(req) & 0xFFFFFF); vocabulary entry v reads word v & 3.
+// One stream of uniforms: key (lo32(seed), hi32(seed)); the block of group g is the output for
+// counter (g, pos, lo32(req), tag << 24 | hi32(req) & 0xFFFFFF).  A scalar draw (ACCEPT) reads
+// word 0 of group 0; race entries use the layout below.
 struct Stream {
   uint32_t k0, k1, pos, req_lo, hi;
 };
@@ -68,7 +69,8 @@ __device__ __forceinline__ uint32_t word_of(const uint4& b, uint32_t lane) {
   return lane == 0 ? b.x : lane == 1 ? b.y : lane == 2 ? b.z : b.w;
 }
 
-// u = ((w >> 9) + 1/2) * 2^-23, exact in binary32, inside (0, 1).
+// The uniform of a scalar draw from word w: u = ((w >> 9) + 1/2) * 2^-23, exact in binary32, inside
+// (0, 1).
 __device__ __forceinline__ float uniform_of(uint32_t w) {
   return (static_cast<float>(w >> 9) + 0.5f) * 1.1920928955078125e-07f;
 }
